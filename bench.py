@@ -1,0 +1,501 @@
+#!/usr/bin/env python
+"""Benchmark of LazyAttention's hot path on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path over one batch of the workload: write the query
+tokens' keys/values into the position-free paged cache, the causal query prefill (keys rotated
+by their document offset), then every decode step (write the new token, attend with Q rotated
+at document boundaries).  The documents were written into the cache once beforehand: that is
+the premise of the method (one cached copy per document, reused at any offset).
+
+Default workload: Llama-3.1-8B attention shape (32/8/128, RoPE theta 5e5), 16 requests x 10
+docs x 200 tokens drawn from a 200-doc pool by Zipf alpha 1.1 and shuffled, 32-token query
+prefill, then 64 decode steps, 16-token pages.  ``--sharing private`` (default) gives every
+(request, doc) its own pages so that logical bytes equal the bytes that must come from HBM;
+``shared`` keeps one physical copy per document.  Inputs are seeded synthetic bf16 N(0,1).
+
+Each step is captured once as a CUDA graph and replayed; L2 is flushed (512 MB write) between
+timed steps, outside the step's own events.  Per-launch decode durations come from event
+records inside the graph, on the launching stream.
+
+``--impl reference`` times the CPU oracle (fp64 NumPy) on a bounded sample per step instead.
+Multi-GPU (torchrun): replicas only -- every rank runs the full workload on its own GPU, no
+collective on the data path; the value is the total over ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode HBM GB/s and prefill TFLOP/s (fraction of GB300 peak); tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_TEXT = {
+    "rag8b": "Llama-3.1-8B attention (32 q / 8 kv heads, D 128, RoPE theta 5e5, bf16); 16 requests "
+             "x 10 docs x 200 tokens from a 200-doc pool by Zipf 1.1, shuffled; 32-token causal "
+             "query prefill then 64 decode steps; 16-token pages",
+    "decode32k": "8B attention shape; 64 requests x 20 docs x 1600 tokens (Zipf 2.1, 500-doc pool); "
+                 "128 decode steps over 32 000-token contexts",
+    "prefill70b": "Llama-3.1-70B attention (64/8/128); 8 requests x 20 docs x 512 tokens (Zipf 1.5) "
+                  "+ 64-token causal query prefill",
+    "mqa_alibi": "MQA 32/1/128 with ALiBi; 32 requests x 12 docs x 1000 tokens, 32-token prefill, "
+                 "64 decode steps",
+    "yarn8b": "8B shape with YaRN (s 8, L0 8192); 32 requests x 12 docs x 1000 tokens, 32-token "
+              "prefill, 64 decode steps",
+    "tiny": "1 request, 4/2 heads, D 64; docs of 48 + 80 tokens; 16-token prefill, 8 decode steps",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="rag8b")
+    p.add_argument("--sharing", choices=["private", "shared"], default="private")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
+    p.add_argument("--pos", default=None, help="override positional kind (e.g. none for the Delta=0 twin)")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+class Dist:
+    def __init__(self):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 7:
+                    try:
+                        rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+                    except ValueError:
+                        pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel_src: str, name: str):
+    """Per-launch DRAM bytes recorded by an ncu capture in profiles/<name>, valid only while
+    the kernel source still hashes to the value recorded there."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    with open(os.path.join(ROOT, "position_agnostic_kv_gb300", "csrc", kernel_src), "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    text = open(path).read()
+    m_h = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_t = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
+    if not m_h or not m_t or m_h.group(1) != h:
+        return None
+    return float(m_t.group(1))
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, dist):
+    import numpy as np
+    import torch
+
+    import position_agnostic_kv_gb300 as lk
+    from position_agnostic_kv_gb300.runner import PagedBatch
+    from workloads import make_workload
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    w = make_workload(args.workload, sharing=args.sharing)
+    pb = PagedBatch(w, device=dev, pos_kind=args.pos)
+    pb.fill_documents()
+    torch.cuda.synchronize()
+    n_dec = w.n_decode
+    pre = pb.upload_prefill() if pb.total_q else None
+    decs = [pb.upload_decode(t) for t in range(n_dec)]
+    out_p = torch.empty((max(pb.total_q, 1), w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    outs_d = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev) for _ in range(n_dec)]
+    stream = torch.cuda.Stream(device=dev)
+    use_graph = not args.no_graph
+
+    def mk():
+        return torch.cuda.Event(enable_timing=True, external=True) if use_graph else \
+            torch.cuda.Event(enable_timing=True)
+
+    ev_pre = (mk(), mk())
+    ev_dec = [(mk(), mk()) for _ in range(n_dec)]
+    launches = 0
+
+    def step():
+        nonlocal launches
+        launches = 0
+        if pre is not None:
+            lk.kv_write(pre["k"], pre["v"], pre["slot"], pre["lp"], pb.k_cache, pb.v_cache, pb.cfg,
+                        stream=stream)
+            ev_pre[0].record(stream)
+            lk.attn_prefill(pre["q"], pb.cu_q, pb.q_start, pb.doc_blocks, pb.meta, pb.k_cache,
+                            pb.v_cache, pb.cfg, out_p[: pb.total_q], pb.max_q, ws=pb.ws, stream=stream)
+            ev_pre[1].record(stream)
+            launches += 1 + launches_of("prefill", pb)
+        for t in range(n_dec):
+            d = decs[t]
+            lk.kv_write(d["k"], d["v"], d["slot"], d["lp"], pb.k_cache, pb.v_cache, pb.cfg, stream=stream)
+            ev_dec[t][0].record(stream)
+            lk.attn_decode(d["q"], d["seq_len"], pb.q_start, pb.doc_blocks, pb.meta, pb.k_cache,
+                           pb.v_cache, pb.cfg, outs_d[t], ws=pb.ws, stream=stream)
+            ev_dec[t][1].record(stream)
+            launches += 1 + launches_of("decode", pb)
+
+    # warm-up (also sets kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            torch.cuda.synchronize()
+        except Exception as e:  # graph capture unsupported here: launch eagerly
+            print(f"[bench] graph capture failed ({e}); launching eagerly", file=sys.stderr)
+            graph = None
+
+    def run_step():
+        with torch.cuda.stream(stream):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+
+    for _ in range(args.warmup):
+        run_step()
+    torch.cuda.synchronize()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dec_ms, pre_ms, step_ms = [], [], []
+    clocks = Clocks(dist.local_rank)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    inner_ok = True
+    for k in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0[k].record(stream)
+            run_step()
+            e1[k].record(stream)
+        stream.synchronize()
+        step_ms.append(e0[k].elapsed_time(e1[k]))
+        if inner_ok:
+            try:
+                if pre is not None:
+                    pre_ms.append(ev_pre[0].elapsed_time(ev_pre[1]))
+                dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
+            except RuntimeError as e:
+                print(f"[bench] in-graph event timing unavailable ({e})", file=sys.stderr)
+                inner_ok = False
+                pre_ms, dec_ms = [], []
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    dist.barrier()
+    clk = clocks.stop()
+    if not inner_ok:  # per-launch times from eager launches of the same step, L2 flushed
+        eager = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n_dec + 1)]
+        for _ in range(min(args.steps, 10)):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                step()
+            stream.synchronize()
+            pre_ms.append(ev_pre[0].elapsed_time(ev_pre[1]) if pre is not None else 0.0)
+            dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
+    status = lk.device_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed region")
+
+    tokens_per_step = pb.total_q + w.B * n_dec
+    mean_ms = dist.max(sum(step_ms) / len(step_ms))
+    value = dist.world * tokens_per_step / (mean_ms / 1e3)
+
+    # algorithmic units (sizes only): decode bytes per launch, prefill flops per launch
+    keys0 = pb.seq_len0_h.astype(np.int64)
+    kv_row = w.Hkv * w.D * 2 * 2
+    dec_bytes = []
+    for t in range(n_dec):
+        keys = keys0 + t + 1
+        blocks = pb.doc_blocks_h.astype(np.int64) + (keys - 1 - pb.q_start_h) // 16 + 1
+        dec_bytes.append(int(keys.sum()) * kv_row + 2 * w.B * w.Hq * w.D * 2 + int(blocks.sum()) * 8)
+    avg_dec_bytes = sum(dec_bytes) / max(n_dec, 1)
+    avg_dec_ms = statistics.mean(dec_ms) if dec_ms else float("nan")
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved_gbs = avg_dec_bytes / (avg_dec_ms / 1e3) / 1e9 if dec_ms else None
+    pre_flops = 0
+    if pb.total_q:
+        for b in range(w.B):
+            L = int(w.q_len[b])
+            pre_flops += 4 * w.D * w.Hq * sum(int(pb.q_start_h[b]) + i + 1 for i in range(L))
+    pre_med = statistics.median(pre_ms) if pre_ms else None
+    pre_tflops = pre_flops / (pre_med / 1e3) / 1e12 if pre_med else None
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    traffic_name = f"decode_{args.workload}_{args.sharing}.md"
+    traffic = profiled_traffic("decode.cu", traffic_name)
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; Zipf-drawn documents)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                   "sharing": args.sharing, "pos": args.pos or w.pos.kind,
+                   "global_batch": w.B * dist.world, "seq_len": int(keys0.max()) + n_dec,
+                   "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{dist.world}",
+                   "l2": "flushed between timed steps (512 MB write, outside the step events)",
+                   "launch": "CUDA graph per step" if graph is not None else "eager"},
+        "roofline": {"kernel": "lazy_attn_decode (split-KV decode + lse merge)", "bound": "hbm",
+                     "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": (achieved_gbs / hbm_peak) if achieved_gbs else None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                     "algorithmic_bytes_per_launch": avg_dec_bytes, "avg_launch_us": avg_dec_ms * 1e3},
+        "prefill": {"kernel": "lazy_attn_prefill", "flops_per_launch": pre_flops,
+                    "median_us": pre_med * 1e3 if pre_med else None, "tflops": pre_tflops,
+                    "frac_bf16_peak": pre_tflops / bf16_peak if pre_tflops else None,
+                    "peak_source": f"{peak_kind} bf16_tflops"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, pb, pre, decs, out_p, outs_d, graph, run_step, stream, dist, tokens_per_step)
+    return res
+
+
+def launches_of(phase: str, pb) -> int:
+    """Kernels one attention call launches: the attention kernel, plus the lse merge when the
+    KV sequence is split (workspace needed)."""
+    import position_agnostic_kv_gb300 as lk
+    if phase == "decode":
+        ws = lk.workspace_size(lk.PHASE_DECODE, pb.B, pb.B, pb.max_blocks, pb.Hq, pb.Hkv, pb.D)
+    else:
+        ws = lk.workspace_size(lk.PHASE_PREFILL, pb.total_q, pb.B, pb.max_blocks, pb.Hq, pb.Hkv, pb.D)
+    return 1 + (1 if ws > 0 else 0)
+
+
+def run_e2e(args, pb, pre, decs, out_p, outs_d, graph, run_step, stream, dist, tokens_per_step):
+    """Same step, but every step's inputs start in pinned host memory and its outputs return
+    to pinned host memory: host->device copies, the step, device->host copies, all timed."""
+    import torch
+    host_in = []
+    for d in ([pre] if pre is not None else []) + decs:
+        host_in.append({k: v.cpu().pin_memory() for k, v in d.items()})
+    dev_in = ([pre] if pre is not None else []) + decs
+    outs = ([out_p[: pb.total_q]] if pre is not None else []) + outs_d
+    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    times = []
+    n = max(3, min(args.steps, 50))
+    for k in range(n + 2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for hd, dd in zip(host_in, dev_in):
+                for key in dd:
+                    dd[key].copy_(hd[key], non_blocking=True)
+            run_step()
+            for ho, o in zip(host_out, outs):
+                ho.copy_(o, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        if k >= 2:
+            times.append(e0.elapsed_time(e1))
+    ms = dist.max(statistics.mean(times))
+    return {"value": dist.world * tokens_per_step / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": n, "api": "position_agnostic_kv_gb300 binding over liblazykv (C ABI), pinned host buffers"}
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+def oracle_sample(w, reqs, n_dec):
+    """Prepare the oracle's caches for `reqs` (setup, untimed) and return a closure that runs
+    one bounded sample of the step for them: KV write of their query tokens, their prefill rows,
+    then n_dec decode steps."""
+    import numpy as np
+    import oracle
+    shape = (w.num_pages, w.Hkv, oracle.PAGE, w.D)
+    kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    pos = w.pos.as_dict()
+    for b in reqs:
+        for i in w.req_inst[w.req_inst_off[b]:w.req_inst_off[b + 1]]:
+            k, v = w.doc_kv(int(w.inst_doc[i]))
+            slot, lp = w.inst_slots(int(i))
+            oracle.kv_write(k, v, slot, lp, pos, kc, vc)
+    _, meta, seq_len, q_start, doc_blocks = oracle.build_meta(
+        w.req_inst_off, w.req_inst, w.inst_len, w.inst_page_off, w.inst_pages, w.q_len,
+        w.q_page_off, w.q_pages, w.max_blocks)
+    q, k, v, slot, lp = w.prefill_tokens()
+    rows = np.concatenate([np.arange(w.cu_q[b], w.cu_q[b + 1]) for b in reqs]) if len(slot) else np.zeros(0, int)
+    decs = [w.decode_tokens(t) for t in range(n_dec)]
+    tokens = len(rows) + n_dec * len(reqs)
+
+    def run():
+        if len(rows):
+            oracle.kv_write(k[rows], v[rows], slot[rows], lp[rows], pos, kc, vc)
+            oracle.prefill(q, w.cu_q, q_start, doc_blocks, meta, kc, vc, pos, requests=reqs)
+        for t, (qd, kd, vd, sd, lpd) in enumerate(decs):
+            oracle.kv_write(kd[reqs], vd[reqs], sd[reqs], lpd[reqs], pos, kc, vc)
+            oracle.decode(qd, seq_len + t + 1, q_start, doc_blocks, meta, kc, vc, pos, requests=reqs)
+    return run, tokens
+
+
+def cpu_baseline(args):
+    from workloads import make_workload
+    w = make_workload(args.workload, sharing=args.sharing)
+    reqs = list(range(min(w.B, 8)))
+    n_dec = min(w.n_decode, 16)
+    run, tokens = oracle_sample(w, reqs, n_dec)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{len(reqs)} requests of {args.workload}: their query prefill + {n_dec} decode "
+                      f"steps ({tokens} tokens, {dt:.1f} s, NumPy fp64, BLAS threads = all cores)"}
+
+
+def run_reference(args, dist):
+    """The oracle as the reference arm: each step = one bounded sample of the workload."""
+    from workloads import make_workload
+    w = make_workload(args.workload, sharing=args.sharing)
+    reqs = [0]
+    n_dec = min(w.n_decode, 2)
+    run, tokens = oracle_sample(w, reqs, n_dec)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    ms = statistics.mean(times) * 1e3
+    value = tokens / (ms / 1e3)
+    cores = len(os.sched_getaffinity(0))
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16; Zipf-drawn documents)",
+            "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
+                       "sharing": args.sharing, "sample_per_step": f"request 0: query prefill + {n_dec} decode steps"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"request 0 of {args.workload}: prefill + {n_dec} decode steps ({tokens} tokens) per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        class _D:  # no process group for the CPU arm
+            world = int(os.environ.get("WORLD_SIZE", "1"))
+        print(json.dumps(run_reference(args, _D())), flush=True)
+        return
+    dist = Dist()
+    try:
+        res = run_ours(args, dist)
+        if dist.rank == 0:
+            if dist.world == 1 and not args.no_cpu_baseline:
+                res["cpu_baseline"] = cpu_baseline(args)
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,31 @@
+// Arguments of the split-KV decode kernel (also used for the per-row prefill path).
+#pragma once
+
+#include "common.cuh"
+
+namespace lazykv {
+
+struct DecodeArgs {
+  const __nv_bfloat16* q;
+  const int32_t* seq_len;
+  const int32_t* cu_q;
+  const int32_t* q_start;
+  const int32_t* doc_blocks;
+  const uint64_t* meta;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  int num_pages, B, max_blocks, Hq, Hkv, rows;
+  int group;  // query heads per CTA (divides Hq / Hkv)
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;   // [rows][Hq][S][D]
+  float* part_ml;  // [rows][Hq][S][2]
+  int S;
+  uint32_t* status;
+  PosParams pos;
+};
+
+int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_bytes, cudaStream_t st);
+size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks);
+
+}  // namespace lazykv

@@ -1,0 +1,282 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Inputs are the seeded workloads; the oracle computes from the same bf16 bits with its own KV
+write (fp64 rotation, one rounding to bf16) and its own block words.  Attention outputs must
+meet max-abs 2e-2, mean-abs 2e-3 and relative 1e-2 (see tests/gpu_common.py); the stored K must
+be within one bf16 unit in the last place of the oracle's and the stored V bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import lazy_oracle as lo
+from tests.gpu_common import (assert_close, lib, oracle_caches_for, request_instances)
+from tests.oracle_setup import oracle_meta, raw_segments
+from workloads import PosCfg, make_custom, make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lk():
+    return lib()
+
+
+def _batch(w, **kw):
+    from position_agnostic_kv_gb300.runner import PagedBatch
+    return PagedBatch(w, device="cuda", **kw)
+
+
+def _bits(t):
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _status_clean(lk):
+    assert lk.device_status() == 0
+
+
+# ------------------------------------------------------------------ cos/sin table
+@pytest.mark.parametrize("kind", ["rope", "yarn"])
+def test_rope_table_matches_fp64(lk, kind):
+    import torch
+    D, max_pos = 128, 40000
+    if kind == "rope":
+        cfg = lk.pos_cfg_from("rope", D, rope_theta=5e5)
+        inv = lo.rope_inv_freq(D, 5e5)
+    else:
+        cfg = lk.pos_cfg_from("yarn", D, rope_theta=5e5, yarn_factor=8.0, yarn_orig_ctx=8192)
+        inv = lo.yarn_inv_freq(D, 5e5, 8.0, 8192)
+    out = torch.empty((max_pos, D), dtype=torch.float32, device="cuda")
+    lk.build_rope_table(cfg, max_pos, out)
+    got = out.cpu().numpy().astype(np.float64)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    # exact angle reduction: error ~2^-25 turn plus one ulp of sin/cos
+    np.testing.assert_allclose(got[:, : D // 2], np.cos(ang), atol=1e-6, rtol=0)
+    np.testing.assert_allclose(got[:, D // 2:], np.sin(ang), atol=1e-6, rtol=0)
+    _status_clean(lk)
+
+
+# ------------------------------------------------------------------ kv write
+@pytest.mark.parametrize("name", ["tiny", "rag8b", "yarn8b", "mqa_alibi"])
+def test_kv_write_parity(lk, name):
+    import torch
+    w = make_workload(name, batch=4)
+    pb = _batch(w)
+    pb.fill_documents()
+    pb.prefill(pb.upload_prefill())
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    kc, vc = oracle_caches_for(w)
+    np.testing.assert_array_equal(_bits(pb.v_cache), vc)
+    gk = lo.bf16_bits_to_f64(_bits(pb.k_cache))
+    rk = lo.bf16_bits_to_f64(kc)
+    # The kernel rotates in fp32 with cos/sin good to ~5e-7 absolute, so before its single
+    # rounding the value is within 5e-7 * (|k1| + |k2|) + 2^-23 |y| of the exact one; after
+    # rounding it is within one bf16 ulp of the oracle's plus that absolute term, which only
+    # matters where the two products nearly cancel (|y| << |k|).  |k| <= 6 for these inputs.
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(rk), 2.0 ** -126))) - 7)
+    bad = np.abs(gk - rk) > ulp + 6e-6
+    assert not bad.any(), f"{bad.sum()} stored K values beyond one bf16 ulp + 6e-6"
+    frac = np.mean(gk != rk)
+    assert frac < 0.01, f"{frac:.4f} of stored K differ from the oracle's rounding"
+
+
+# ------------------------------------------------------------------ attention
+def _run_and_check(lk, w, reqs, n_steps, check_steps, use_table=False, sharpen=1.0):
+    """Run fill -> prefill -> n_steps decode steps on the GPU; compare prefill rows of `reqs`
+    and the decode outputs of `reqs` at `check_steps` against the oracle."""
+    import torch
+    pb = _batch(w, use_table=use_table)
+    pb.fill_documents()
+    inp = pb.upload_prefill()
+    if sharpen != 1.0:
+        inp["q"] = (inp["q"].float() * sharpen).to(torch.bfloat16)
+    out_p = pb.prefill(inp)
+    outs_d = {}
+    for t in range(n_steps):
+        o = pb.decode_step(pb.upload_decode(t))
+        if t in check_steps:
+            outs_d[t] = o.clone()
+    torch.cuda.synchronize()
+    _status_clean(lk)
+
+    bt, meta, seq_len, q_start, doc_blocks = oracle_meta(w)
+    np.testing.assert_array_equal(meta, pb.meta_h)
+    pos = w.pos.as_dict()
+    kc, vc = oracle_caches_for(w, request_instances(w, reqs), prefill=True)
+    q = w.prefill_tokens()[0]
+    if sharpen != 1.0:
+        q = _bits(inp["q"])
+    results = {}
+    if w.q_len.sum():
+        ref_p, _ = lo.prefill(q, w.cu_q, q_start, doc_blocks, meta, kc, vc, pos, requests=reqs)
+        rows = np.concatenate([np.arange(w.cu_q[b], w.cu_q[b + 1]) for b in reqs])
+        results["prefill"] = assert_close(out_p[rows], ref_p[rows], f"{w.name} prefill")
+    done = 0
+    for t in sorted(check_steps):
+        while done <= t:
+            _, k, v, slot, lp = w.decode_tokens(done)
+            oracle.kv_write(k, v, slot, lp, pos, kc, vc)
+            done += 1
+        qd = w.decode_tokens(t)[0]
+        ref_d, _ = lo.decode(qd, seq_len + t + 1, q_start, doc_blocks, meta, kc, vc, pos,
+                             requests=reqs)
+        results[f"decode{t}"] = assert_close(outs_d[t][reqs], ref_d[reqs], f"{w.name} decode step {t}")
+    return results
+
+
+def test_tiny_all_steps(lk):
+    w = make_workload("tiny")
+    _run_and_check(lk, w, [0], w.n_decode, set(range(w.n_decode)))
+
+
+def test_tiny_matches_materialized_definition(lk):
+    """End to end against the definition itself: keys rotated straight to absolute positions
+    from the raw bf16 inputs (no position-free cache anywhere on the oracle side)."""
+    import torch
+    w = make_workload("tiny")
+    pb = _batch(w)
+    pb.fill_documents()
+    out_p = pb.prefill(pb.upload_prefill())
+    q = w.prefill_tokens()[0]
+    _, _, sl, qs, _ = oracle_meta(w)
+    m = qs[0] + np.arange(w.q_len[0])
+    ref, _ = lo.materialized_attention(raw_segments(w, 0, 0), lo.as_f64(q), m, w.pos.as_dict())
+    assert_close(out_p, ref, "tiny prefill vs materialised")
+    for t in range(w.n_decode):
+        o = pb.decode_step(pb.upload_decode(t))
+        qd = w.decode_tokens(t)[0]
+        ref, _ = lo.materialized_attention(raw_segments(w, 0, t + 1), lo.as_f64(qd),
+                                           [sl[0] + t], w.pos.as_dict())
+        assert_close(o, ref, f"tiny decode {t} vs materialised")
+    torch.cuda.synchronize()
+    _status_clean(lk)
+
+
+@pytest.mark.parametrize("sharing", ["shared", "private"])
+def test_rag8b(lk, sharing):
+    w = make_workload("rag8b", sharing=sharing)
+    _run_and_check(lk, w, [0, 5, 15], 4, {0, 3})
+
+
+def test_rag8b_table_mode(lk):
+    w = make_workload("rag8b")
+    _run_and_check(lk, w, [1, 7], 3, {2}, use_table=True)
+
+
+def test_yarn8b(lk):
+    w = make_workload("yarn8b")
+    _run_and_check(lk, w, [0, 31], 3, {0, 2})
+
+
+def test_mqa_alibi(lk):
+    w = make_workload("mqa_alibi")
+    _run_and_check(lk, w, [0, 13], 3, {0, 2})
+
+
+def test_prefill70b(lk):
+    w = make_workload("prefill70b")
+    _run_and_check(lk, w, list(range(w.B)), 0, set())
+
+
+def test_decode32k(lk):
+    """Full decode-bound workload (64 requests, 32 000-token contexts, 128 steps) on the GPU;
+    the oracle checks four requests at steps 0, 63 and 127."""
+    w = make_workload("decode32k")
+    _run_and_check(lk, w, [0, 21, 42, 63], 128, {0, 63, 127})
+
+
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 4), (64, 8, 2), (128, 8, 1), (128, 16, 2), (64, 16, 2)])
+def test_edge_shapes(lk, D, Hq, Hkv):
+    """Documents of 1, 15, 16, 17 and 33 tokens, uneven query lengths (one request without a
+    query segment), MHA / GQA / MQA groupings and both head dims."""
+    w = make_custom([1, 15, 16, 17, 33], [[4, 0, 2], [1, 3], [2, 4, 1, 0]], Hq, Hkv, D,
+                    PosCfg("rope", 1e4, D), [3, 0, 17], 5, seed=D + Hq)
+    _run_and_check(lk, w, [0, 1, 2], 5, {0, 4})
+
+
+def test_sharpened_queries_separate_negative_controls(lk):
+    """With queries x4 the softmax is sharp: the GPU output must match the oracle, while the
+    oracle run with wrong offsets (Delta = 0 everywhere, Delta + 1, the naive double rotation
+    2*Delta) misses the GPU output by more than the tolerance."""
+    import torch
+    w = make_workload("rag8b", batch=2)
+    pb = _batch(w)
+    pb.fill_documents()
+    inp = pb.upload_prefill()
+    inp["q"] = (inp["q"].float() * 4.0).to(torch.bfloat16)
+    out = pb.prefill(inp)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    q4 = _bits(inp["q"])
+    _, meta, _, qs, db = oracle_meta(w)
+    kc, vc = oracle_caches_for(w)
+    pos = w.pos.as_dict()
+    ref, _ = lo.prefill(q4, w.cu_q, qs, db, meta, kc, vc, pos)
+    assert_close(out, ref, "sharpened prefill")
+    for fn in (lambda d: 0, lambda d: d + 1, lambda d: 2 * d):
+        bad = meta.copy()
+        for b in range(w.B):
+            for j in range(meta.shape[1]):
+                nv, pg, dl, page = lo.unpack_meta(int(meta[b, j]))
+                if nv:
+                    bad[b, j] = lo.pack_meta(nv, pg, fn(dl), page)
+        wrong, _ = lo.prefill(q4, w.cu_q, qs, db, bad, kc, vc, pos)
+        err = np.abs(out.float().cpu().numpy() - wrong).max()
+        assert err > 2e-2, f"negative control not separated: {err:.3e}"
+
+
+def test_no_rotation_twin(lk):
+    """The 'Delta = 0' twin (POS_NONE) computes plain attention with no positional term: it
+    equals the oracle's ALiBi path with zero slopes (which rotates nothing)."""
+    import torch
+    w = make_workload("rag8b", batch=3)
+    pb = _batch(w, pos_kind="none")
+    pb.fill_documents()
+    out_p = pb.prefill(pb.upload_prefill())
+    out_d = pb.decode_step(pb.upload_decode(0))
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    pos = dict(kind="alibi", alibi_slopes=np.zeros(w.Hq))
+    shape = (w.num_pages, w.Hkv, 16, w.D)
+    kc, vc = np.zeros(shape, np.uint16), np.zeros(shape, np.uint16)
+    for i in range(len(w.inst_doc)):
+        k, v = w.doc_kv(int(w.inst_doc[i]))
+        slot, lp = w.inst_slots(i)
+        lo.kv_write(k, v, slot, lp, pos, kc, vc)
+    q, k, v, slot, lp = w.prefill_tokens()
+    lo.kv_write(k, v, slot, lp, pos, kc, vc)
+    _, meta, sl, qs, db = oracle_meta(w)
+    ref_p, _ = lo.prefill(q, w.cu_q, qs, db, meta, kc, vc, pos, scale=1 / np.sqrt(w.D))
+    assert_close(out_p, ref_p, "no-rotation prefill")
+    qd, kd, vd, sd, lpd = w.decode_tokens(0)
+    lo.kv_write(kd, vd, sd, lpd, pos, kc, vc)
+    ref_d, _ = lo.decode(qd, sl + 1, qs, db, meta, kc, vc, pos, scale=1 / np.sqrt(w.D))
+    assert_close(out_d, ref_d, "no-rotation decode")
+
+
+def test_bad_page_sets_status_and_skips(lk):
+    """A block word naming a page beyond the cache is caught by the kernel's bounds check:
+    the status word gets LAZY_STATUS_BAD_PAGE and the page is skipped (no access)."""
+    import torch
+    w = make_workload("tiny")
+    pb = _batch(w)
+    pb.fill_documents()
+    bad = pb.meta_h.copy()
+    nv, pg, dl, _ = lo.unpack_meta(int(bad[0, 1]))
+    bad[0, 1] = lo.pack_meta(nv, pg, dl, w.num_pages + 5)
+    pb.meta = torch.from_numpy(bad.view(np.int64)).cuda()
+    pb.prefill(pb.upload_prefill())
+    st = lk.device_status()
+    assert st & 1, st
+    assert lk.device_status() == 0  # cleared by the read
+
+
+def test_workspace_too_small_is_rejected(lk):
+    import torch
+    w = make_workload("rag8b", batch=16)
+    pb = _batch(w)
+    pb.ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lk.LazyError, match="workspace"):
+        pb.decode_step(pb.upload_decode(0))
