@@ -160,6 +160,32 @@ int lazy_attn_decode(const void* q, const int32_t* seq_len, const int32_t* q_sta
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * lazy_attn_decode_noalloc -- lazy_attn_decode for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is a deployment variant of the decode above.
+ *
+ * Who needs it: a host that owns all GPU memory itself (e.g. an engine that reserves HBM for
+ * its KV pool at start-up and gives plugins no allocator), or a latency-bound loop that must
+ * never call cudaMalloc (which can synchronise the device).  Such callers cannot pass the
+ * split-KV workspace lazy_attn_decode needs, so this entry point uses a fixed 16 MiB array
+ * compiled into the library instead; neither the caller nor the library allocates (no
+ * cudaMalloc, cudaFree or allocating library routine is called).
+ *   Arguments, layouts and results: exactly those of lazy_attn_decode, without ws/ws_bytes.
+ *   Limit: batches whose split scratch (see lazy_workspace_size) exceeds 16 MiB are rejected
+ *          with LAZY_EINVAL and a message; nothing is launched.
+ *   Memory: every GPU that loads the library holds the 16 MiB array until the process exits.
+ *   Set-up: the first call on each device looks up the array's device address (with that
+ *          device current); make that first call before any stream capture.
+ *   Sharing: all calls on a device share the one array and it keeps the last call's contents.
+ *          Nothing in it must start at zero.  Calls that overlap on the GPU (different
+ *          streams, or different host threads) race on it: serialise them.
+ */
+int lazy_attn_decode_noalloc(const void* q, const int32_t* seq_len, const int32_t* q_start,
+                             const int32_t* doc_blocks, const uint64_t* meta, int B,
+                             int max_blocks, const void* k_cache, const void* v_cache,
+                             int num_pages, int Hq, int Hkv, int D, float scale,
+                             const lazy_pos_cfg* cfg, void* out, float* lse, void* stream);
+
+/*
  * lazy_attn_prefill -- causal prefill of every request's query tokens over its documents and
  * its own earlier tokens.  [NOTE] Tiling 感知: prefill rotates each K tile by its document's
  * Delta (Q tiles are much taller than K tiles); [NOTE] 融合 Triton kernel (K tile split in

@@ -18,14 +18,14 @@ import numpy as np
 
 __all__ = ["LIB_PATH", "lib", "PosCfg", "LazyError", "POS_ROPE", "POS_YARN", "POS_ALIBI",
            "POS_NONE", "PHASE_DECODE", "PHASE_PREFILL", "EXPORTED_SYMBOLS", "build_doc_meta",
-           "build_rope_table", "kv_write", "attn_decode", "attn_prefill", "workspace_size",
+           "build_rope_table", "kv_write", "attn_decode", "attn_decode_noalloc", "attn_prefill", "workspace_size",
            "device_status", "pos_cfg_from"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblazykv.so")
 POS_ROPE, POS_YARN, POS_ALIBI, POS_NONE = 0, 1, 2, 3
 PHASE_DECODE, PHASE_PREFILL = 0, 1
 EXPORTED_SYMBOLS = ("lazy_build_doc_meta", "lazy_build_rope_table", "lazy_kv_write",
-                    "lazy_attn_decode", "lazy_attn_prefill", "lazy_workspace_size",
+                    "lazy_attn_decode", "lazy_attn_decode_noalloc", "lazy_attn_prefill", "lazy_workspace_size",
                     "lazy_device_status", "lazy_last_error", "lazy_version")
 
 if not os.path.exists(LIB_PATH):
@@ -56,6 +56,8 @@ _sig = {
     "lazy_kv_write": [_P, _P, _P, _P, _I, _I, _I, _P, _P, _I, ctypes.POINTER(PosCfg), _P],
     "lazy_attn_decode": [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, ctypes.c_float,
                          ctypes.POINTER(PosCfg), _P, _P, _P, _SZ, _P],
+    "lazy_attn_decode_noalloc": [_P, _P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I,
+                                 ctypes.c_float, ctypes.POINTER(PosCfg), _P, _P, _P],
     "lazy_attn_prefill": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _I, _I,
                           ctypes.c_float, ctypes.POINTER(PosCfg), _P, _P, _P, _SZ, _P],
     "lazy_workspace_size": [_I, _I, _I, _I, _I, _I, _I],
@@ -197,6 +199,29 @@ def attn_decode(q, seq_len, q_start, doc_blocks, meta, k_cache, v_cache, cfg: Po
                                 _dev_ptr(out, torch.bfloat16, "out"),
                                 _dev_ptr(lse, torch.float32, "lse"), wsp, wsb, _stream(stream)),
            "lazy_attn_decode")
+
+
+def attn_decode_noalloc(q, seq_len, q_start, doc_blocks, meta, k_cache, v_cache, cfg: PosCfg,
+                        out, lse=None, scale: float = 0.0, stream=None):
+    """``attn_decode`` without a workspace: for callers that cannot allocate device memory.
+    The split scratch lives in a fixed 16 MiB array inside the library (one per GPU), shared by
+    all calls on that device; calls that overlap on the GPU race on it.  The first call on a
+    device looks up the array's address, so make it before any stream capture."""
+    import torch
+    B, Hq, D = q.shape
+    if tuple(out.shape) != (B, Hq, D) or meta.shape[0] != B:
+        raise ValueError("attn_decode_noalloc: inconsistent shapes")
+    _check(lib.lazy_attn_decode_noalloc(_dev_ptr(q, torch.bfloat16, "q"),
+                                        _dev_ptr(seq_len, torch.int32, "seq_len"),
+                                        _dev_ptr(q_start, torch.int32, "q_start"),
+                                        _dev_ptr(doc_blocks, torch.int32, "doc_blocks"),
+                                        _dev_ptr(meta, None, "meta"), B, meta.shape[1],
+                                        _dev_ptr(k_cache, torch.bfloat16, "k_cache"),
+                                        _dev_ptr(v_cache, torch.bfloat16, "v_cache"),
+                                        k_cache.shape[0], Hq, k_cache.shape[1], D, scale,
+                                        ctypes.byref(cfg), _dev_ptr(out, torch.bfloat16, "out"),
+                                        _dev_ptr(lse, torch.float32, "lse"), _stream(stream)),
+           "lazy_attn_decode_noalloc")
 
 
 def attn_prefill(q, cu_q, q_start, doc_blocks, meta, k_cache, v_cache, cfg: PosCfg, out,
