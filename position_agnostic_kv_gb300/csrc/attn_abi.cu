@@ -69,6 +69,11 @@ extern "C" int lazy_attn_prefill(const void* q, const int32_t* cu_q, const int32
   DecodeArgs a = {};
   rc = prepare_pos(cfg, Hq, D, scale, &a.pos);
   if (rc) return rc;
+  const int G = Hq / Hkv;
+  if (G <= 128 && 128 % G == 0)  // tensor-core path: 128 GQA-packed query rows per CTA
+    return run_prefill_tc(q, cu_q, q_start, doc_blocks, meta, B, max_blocks, max_q, k_cache, v_cache, num_pages,
+                          Hq, Hkv, D, a.pos, out, lse, static_cast<cudaStream_t>(stream));
+  // other head groupings: one CTA per query row on CUDA cores (the decode kernel's row mode)
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.seq_len = nullptr;
   a.cu_q = cu_q;
@@ -92,6 +97,9 @@ extern "C" int lazy_attn_prefill(const void* q, const int32_t* cu_q, const int32
 extern "C" size_t lazy_workspace_size(int phase, int rows, int B, int max_blocks, int Hq, int Hkv, int D) {
   (void)B;
   if (rows <= 0 || max_blocks <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
-  if (phase != LAZY_PHASE_DECODE && phase != LAZY_PHASE_PREFILL) return 0;
+  if (phase == LAZY_PHASE_DECODE) return decode_ws_bytes(rows, Hq, Hkv, D, max_blocks);
+  if (phase != LAZY_PHASE_PREFILL) return 0;
+  const int G = Hq / Hkv;
+  if (G <= 128 && 128 % G == 0) return 0;  // the tensor-core prefill needs no workspace
   return decode_ws_bytes(rows, Hq, Hkv, D, max_blocks);
 }

@@ -27,5 +27,9 @@ struct DecodeArgs {
 
 int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks);
+int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
+                   const uint64_t* meta, int B, int max_blocks, int max_q, const void* k_cache,
+                   const void* v_cache, int num_pages, int Hq, int Hkv, int D, const PosParams& pos, void* out,
+                   float* lse, cudaStream_t st);
 
 }  // namespace lazykv

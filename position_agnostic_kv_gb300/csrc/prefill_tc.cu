@@ -1,0 +1,697 @@
+// Causal prefill over the position-free paged cache on the 5th-generation tensor cores.
+//
+// [NOTE] Tiling 感知的 Q/K 旋转分派: in prefill the query tile is much taller than a KV tile,
+// so the KV side is rotated: every staged K tile gets one relative rotation R_Delta per
+// document (3 extra flops per K scalar) before the QK^T GEMM.  [NOTE] 融合 Triton kernel:
+// the K tile is split in its two half-dimensions, rotated, then multiplied.  [GIST]
+// Prefilling: a single relative rotation by the offset, never un-rotate then re-rotate.
+//
+// GB300 design (one CTA per (request, KV head, 128 query rows); 320 threads, 1 CTA per SM):
+//   warps 0-3  softmax + epilogue.  Thread r owns TMEM lane r = query row r of the tile.
+//   warps 4-7  Q preparation (rotate by its absolute position m, fold in the softmax scale,
+//              write the 128B-swizzled K-major operand), then for every K tile: rotate each
+//              page's 16 rows by that page's Delta in place, in shared memory, and zero the V
+//              rows that hold no key (so no stale bits reach the tensor core).
+//   warp 8     producer: unpacks the 64-bit block words of the tile's 8 pages and issues TMA
+//              tile loads (box 16 rows x 64 columns, 128-byte swizzle) into a 2-stage ring.
+//   warp 9     TMEM owner and MMA issuer: S = Q K^T (M 128, N 128, K 16 steps) into one of two
+//              TMEM S buffers, then O += P V (P from shared memory, V as an MN-major operand)
+//              into a TMEM accumulator; completion is signalled by tcgen05.commit.
+// GQA: the tile's rows are (token, head) pairs of the KV head's query-head group, token-major,
+// so one K/V tile serves G heads.  Online softmax in base 2; the running max moves (and O is
+// rescaled in TMEM) only when a row's max grows by more than 8.  Every wait is bounded.
+#include <cfloat>
+#include <climits>
+
+#include <cuda.h>  // CUtensorMap and the encoder's types (the function is looked up at run time)
+
+#include "common.cuh"
+
+namespace lazykv {
+
+namespace tc {
+
+constexpr int kM = 128;            // query rows per CTA
+constexpr int kN = 128;            // keys per K/V tile
+constexpr int kPagesPerTile = kN / kPage;
+constexpr int kStages = 2;
+constexpr int kThreads = 320;
+constexpr int kProdWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kTau = 8.0f;
+
+// barrier indices
+enum : int {
+  B_KV_FULL = 0,   // [2] TMA bytes landed
+  B_K_READY = 2,   // [2] K rotated, V cleaned (128 arrivals)
+  B_KV_FREE = 4,   // [2] stage consumed by QK and PV (commit)
+  B_S_FULL = 6,    // [2] S buffer written (commit)
+  B_S_FREE = 8,    // [2] S buffer read (128 arrivals)
+  B_P_FULL = 10,   // P tile written (128 arrivals)
+  B_PV_DONE = 11,  // PV finished (commit)
+  B_Q_READY = 12,  // Q tile prepared (128 arrivals)
+  B_FINAL = 13,    // all MMAs finished (commit)
+  NBAR = 14
+};
+
+template <int D>
+struct Layout {
+  static constexpr int CB = D / 64;                        // 128-byte column blocks per row
+  static constexpr int BLK = kM * 128;                     // one column block of a 128-row tile
+  static constexpr int TILE = kN * D * 2;                  // one K or V tile
+  static constexpr int Q_OFF = 0;
+  static constexpr int P_OFF = Q_OFF + kM * D * 2;
+  static constexpr int ST_OFF = P_OFF + kM * kN * 2;
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int KPOS_OFF = ST_OFF + kStages * STAGE;            // int [stage][128]
+  static constexpr int PINFO_OFF = KPOS_OFF + kStages * kN * 4;         // int2 [stage][8]
+  static constexpr int FLAG_OFF = PINFO_OFF + kStages * kPagesPerTile * 8;
+  static constexpr int CS_OFF = FLAG_OFF + 16;                          // float2 [8][D/2]
+  static constexpr int BAR_OFF = CS_OFF + kPagesPerTile * (D / 2) * 8;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;                   // tmem slot, abort flag
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;                     // + alignment slack
+};
+
+struct Args {
+  const __nv_bfloat16* q;
+  const int32_t* cu_q;
+  const int32_t* q_start;
+  const int32_t* doc_blocks;
+  const uint64_t* meta;
+  int B, max_blocks, Hq, Hkv, num_pages;
+  __nv_bfloat16* out;
+  float* lse;
+  uint32_t* status;
+  PosParams pos;
+};
+
+// ---------------------------------------------------------------- tcgen05 / TMA wrappers
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  // tcgen05 shared-memory matrix descriptor: start>>4, LBO>>4, SBO>>4, version 1,
+  // base offset 0 (1024-byte aligned atoms), 128-byte swizzle.
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// instruction descriptor, kind::f16: fp32 accumulate, A and B both bf16 (ab_f16 = 0) or both
+// f16 (ab_f16 = 1), K-major A, B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_mma(int M, int N, int b_mn, int ab_f16) {
+  return (1u << 4) | (uint32_t(ab_f16 ? 0 : 1) << 7) | (uint32_t(ab_f16 ? 0 : 1) << 10) | (uint32_t(b_mn) << 16) |
+         (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    if ((++n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort_flag = 1;
+        set_status(status, LAZY_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block (1024-byte atoms)
+__device__ __forceinline__ uint32_t swz(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// ---------------------------------------------------------------- the kernel
+template <int D, int POS>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
+  using L = Layout<D>;
+  constexpr bool kRotate = (POS == kRope || POS == kYarn);
+  // With rotation, the rotated Q and K are rounded once more before QK^T: write them as f16
+  // (10 mantissa bits; stored bf16 keys convert exactly) so QK^T runs as an f16 x f16 MMA.
+  // Without rotation K is the stored bf16 itself, so Q is rounded to bf16.  PV is bf16 x bf16.
+  constexpr bool kQkF16 = kRotate;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int G = a.Hq / a.Hkv;
+  const int tpt = kM / G;  // tokens per tile
+  const int q0 = a.cu_q[b];
+  const int Lq = a.cu_q[b + 1] - q0;
+  const int tok0 = mt * tpt;
+  if (tok0 >= Lq) return;  // uniform for the CTA, before any barrier or TMEM use
+  const int qs = a.q_start[b];
+  const int ntok = min(tpt, Lq - tok0);
+  const int m_min = qs + tok0, m_max = qs + tok0 + ntok - 1;
+  int nb = a.doc_blocks[b] + (m_max - qs) / kPage + 1;
+  if (nb > a.max_blocks) {
+    if (threadIdx.x == 0) set_status(a.status, LAZY_STATUS_BAD_ROW);
+    nb = a.max_blocks;
+  }
+  const int ntiles = (nb + kPagesPerTile - 1) / kPagesPerTile;
+
+  const uint32_t sQ = sb + L::Q_OFF, sP = sb + L::P_OFF, sST = sb + L::ST_OFF;
+  int* kpos = reinterpret_cast<int*>(sm + L::KPOS_OFF);
+  int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
+  int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
+  float2* cs = reinterpret_cast<float2*>(sm + L::CS_OFF);
+  const uint32_t bar0 = sb + L::BAR_OFF;
+  auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(BAR(B_KV_FULL + s), 1);
+      mbar_init(BAR(B_K_READY + s), 128);
+      mbar_init(BAR(B_KV_FREE + s), 1);
+      mbar_init(BAR(B_S_FULL + s), 1);
+      mbar_init(BAR(B_S_FREE + s), 128);
+    }
+    mbar_init(BAR(B_P_FULL), 128);
+    mbar_init(BAR(B_PV_DONE), 1);
+    mbar_init(BAR(B_Q_READY), 128);
+    mbar_init(BAR(B_FINAL), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S0 at +0, S1 at +128, O at +256
+
+  if (warp < 4) {
+    // ============================ softmax + epilogue (TMEM lanes 32*warp .. +32)
+    const int r = threadIdx.x;                 // query row of the tile
+    const int token = tok0 + r / G;
+    const int h = g * G + r % G;
+    const bool valid = token < Lq;
+    const int m_row = valid ? qs + token : -1;
+    float slope = 0.f;
+    if constexpr (POS == kAlibi) slope = a.pos.slopes[h] * 1.4426950408889634f;
+    const uint32_t tl = tmem + (uint32_t(32 * warp) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int s = j % kStages, sbuf = j & 1;
+      const bool got_s = wait_bar(BAR(B_S_FULL + sbuf), uint32_t((j >> 1) & 1), abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
+      tc_fence_after();
+      const bool fast = (POS != kAlibi) && flags[s];
+      const int* kp = kpos + s * kN;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c4 = 0; c4 < kN / 32; ++c4) {
+        uint32_t v[32];
+        tmem_ld32(tl + uint32_t(sbuf * kN + c4 * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(v[e]);
+          if (!fast) {
+            const int p = kp[c4 * 32 + e];
+            if constexpr (POS == kAlibi) x += slope * float(p - m_row);
+            x = (p <= m_row) ? x : -INFINITY;
+          }
+          mx = fmaxf(mx, x);
+        }
+      }
+      const bool need = mx > m_run + kTau;
+      const float m_new = need ? mx : m_run;
+      uint32_t pk[kN / 2];
+      float sum = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < kN / 32; ++c4) {
+        uint32_t v[32];
+        tmem_ld32(tl + uint32_t(sbuf * kN + c4 * 32), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+          if (!fast) {
+            const int p0 = kp[c4 * 32 + e], p1 = kp[c4 * 32 + e + 1];
+            if constexpr (POS == kAlibi) {
+              x0 += slope * float(p0 - m_row);
+              x1 += slope * float(p1 - m_row);
+            }
+            x0 = (p0 <= m_row) ? x0 : -INFINITY;
+            x1 = (p1 <= m_row) ? x1 : -INFINITY;
+          }
+          const float e0 = (m_new == -INFINITY) ? 0.f : exp2f(x0 - m_new);
+          const float e1 = (m_new == -INFINITY) ? 0.f : exp2f(x1 - m_new);
+          sum += e0 + e1;
+          pk[c4 * 16 + e / 2] = f2_to_bf2(e0, e1);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(B_S_FREE + sbuf));
+      if (j > 0) {
+        const bool got_pv = wait_bar(BAR(B_PV_DONE), uint32_t((j - 1) & 1), abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, got_pv)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const float alpha = (j > 0 && need && m_run != -INFINITY) ? exp2f(m_run - m_new) : 1.f;
+      l_run = (j == 0) ? sum : l_run * alpha + sum;
+      if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + uint32_t(2 * kN + c * 32), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(tl + uint32_t(2 * kN + c * 32), v);
+        }
+        tmem_wait_st();
+      }
+      m_run = m_new;
+      // P row -> shared memory, K-major, 128-byte swizzle (2 column blocks of 64 keys)
+#pragma unroll
+      for (int cb = 0; cb < kN / 64; ++cb)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          st_shared_v4(sP + uint32_t(cb * L::BLK) + swz(r, c),
+                       make_uint4(pk[cb * 32 + c * 4], pk[cb * 32 + c * 4 + 1], pk[cb * 32 + c * 4 + 2],
+                                  pk[cb * 32 + c * 4 + 3]));
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(BAR(B_P_FULL));
+    }
+    const bool got_last = ok && wait_bar(BAR(B_PV_DONE), uint32_t((ntiles - 1) & 1), abort_flag, a.status);
+    if (__all_sync(0xffffffffu, got_last)) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = a.out + ((size_t)(q0 + token) * a.Hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + uint32_t(2 * kN + c * 32), v);
+        tmem_wait_ld();
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(f2_to_bf2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv),
+                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv),
+                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv),
+                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv));
+        }
+      }
+      if (valid && a.lse) a.lse[(size_t)(q0 + token) * a.Hq + h] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+    }
+  } else if (warp < kProdWarp) {
+    // ============================ Q preparation, K rotation, V cleaning
+    const int rt = threadIdx.x - 128;
+    {
+      const int token = tok0 + rt / G;
+      const int h = g * G + rt % G;
+      const bool valid = token < Lq;
+      float x[D];
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)(q0 + token) * a.Hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 u = src[c];
+          x[c * 8 + 0] = bf_lo(u.x); x[c * 8 + 1] = bf_hi(u.x);
+          x[c * 8 + 2] = bf_lo(u.y); x[c * 8 + 3] = bf_hi(u.y);
+          x[c * 8 + 4] = bf_lo(u.z); x[c * 8 + 5] = bf_hi(u.z);
+          x[c * 8 + 6] = bf_lo(u.w); x[c * 8 + 7] = bf_hi(u.w);
+        }
+        if constexpr (kRotate) {
+          const uint32_t m = uint32_t(qs + token);
+          const bool tab = a.pos.table != nullptr && int(m) < a.pos.max_pos;
+#pragma unroll
+          for (int i = 0; i < D / 2; ++i) {
+            float sn, co;
+            if (tab) {
+              co = a.pos.table[(size_t)m * D + i];
+              sn = a.pos.table[(size_t)m * D + D / 2 + i];
+            } else {
+              turn_sincos(m, a.pos.turns[i], sn, co);
+            }
+            const float x1 = x[i], x2 = x[i + D / 2];
+            x[i] = x1 * co - x2 * sn;
+            x[i + D / 2] = x1 * sn + x2 * co;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < D; ++i) x[i] *= a.pos.scale_log2;
+      } else {
+#pragma unroll
+        for (int i = 0; i < D; ++i) x[i] = 0.f;
+      }
+#pragma unroll
+      for (int cb = 0; cb < L::CB; ++cb)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float* y = x + cb * 64 + c * 8;
+          if constexpr (kQkF16)
+            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(rt, c),
+                         make_uint4(f2_to_h2(y[0], y[1]), f2_to_h2(y[2], y[3]), f2_to_h2(y[4], y[5]),
+                                    f2_to_h2(y[6], y[7])));
+          else
+            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(rt, c),
+                         make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
+                                    f2_to_bf2(y[6], y[7])));
+        }
+      fence_async_smem();
+      mbar_arrive(BAR(B_Q_READY));
+    }
+    const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
+    bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
+      if (ok) ok = wait_bar(BAR(B_KV_FULL + s), uint32_t((j / kStages) & 1), abort_flag, a.status);
+      const int2 pi = ok ? pinfo[s * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, rows}
+      const uint32_t sK = sST + uint32_t(s * L::STAGE), sV = sK + L::TILE;
+      if constexpr (kRotate) {
+        for (int idx = rt; ok && idx < kPagesPerTile * (D / 2); idx += 128) {
+          const int pp = idx / (D / 2), i = idx % (D / 2);
+          float sn, co;
+          turn_sincos(uint32_t(pinfo[s * kPagesPerTile + pp].x), a.pos.turns[i], sn, co);
+          cs[idx] = make_float2(co, sn);
+        }
+        named_sync(1, 128);
+        if (ok && t < pi.y) {
+          const float2* c2 = cs + ps * (D / 2);
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            // pair i = c*8 + e: element i and its partner i + D/2 share the swizzled chunk slot
+            const uint32_t a1 = sK + swz(rt, c);
+            const uint32_t a2 = (D == 128) ? sK + uint32_t(L::BLK) + swz(rt, c) : sK + swz(rt, c + 4);
+            uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
+            uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
+            uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float2 cA = c2[c * 8 + 2 * w], cB = c2[c * 8 + 2 * w + 1];
+              const float x1a = bf_lo(p1[w]), x1b = bf_hi(p1[w]);
+              const float x2a = bf_lo(p2[w]), x2b = bf_hi(p2[w]);
+              p1[w] = f2_to_h2(x1a * cA.x - x2a * cA.y, x1b * cB.x - x2b * cB.y);
+              p2[w] = f2_to_h2(x1a * cA.y + x2a * cA.x, x1b * cB.y + x2b * cB.x);
+            }
+            st_shared_v4(a1, u1);
+            st_shared_v4(a2, u2);
+          }
+        }
+      }
+      if (ok && t >= pi.y) {  // no key in this row: clear V so no stale bits reach the MMA
+#pragma unroll
+        for (int cb = 0; cb < L::CB; ++cb)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(rt, c), make_uint4(0, 0, 0, 0));
+      }
+      fence_async_smem();
+      if constexpr (kRotate) named_sync(1, 128);  // cos/sin table reused next tile
+      mbar_arrive(BAR(B_K_READY + s));
+    }
+  } else if (warp == kProdWarp) {
+    // ============================ block words + TMA
+    const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages) {
+        const bool freed = wait_bar(BAR(B_KV_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, freed)) break;
+      }
+      int rows = 0, start = 0, page = 0, delta = 0;
+      const int jb = j * kPagesPerTile + lane;
+      if (lane < kPagesPerTile && jb < nb) {
+        const uint64_t w = ldg_u64(mrow + jb);
+        page = int(word_page(w));
+        delta = int(word_delta(w));
+        start = delta + kPage * int(word_pg(w));
+        rows = min(int(word_nvalid(w)), kPage);
+        if (page >= a.num_pages) {
+          set_status(a.status, LAZY_STATUS_BAD_PAGE);
+          rows = 0;
+        }
+      }
+      if (lane < kPagesPerTile) pinfo[s * kPagesPerTile + lane] = make_int2(delta, rows);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int idx = lane * 4 + e, pp = idx >> 4, tt = idx & 15;
+        const int rp = __shfl_sync(0xffffffffu, rows, pp);
+        const int sp = __shfl_sync(0xffffffffu, start, pp);
+        kpos[s * kN + idx] = tt < rp ? sp + tt : INT_MAX;
+      }
+      const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
+      const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
+      if (lane == 0) flags[s] = all16 && (last_start + kPage - 1 <= m_min);
+      __syncwarp();
+      uint32_t bytes = 0;
+      for (int pp = 0; pp < kPagesPerTile; ++pp)
+        if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += 2u * kPage * D * 2;
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_KV_FULL + s), bytes);
+      for (int pp = 0; pp < kPagesPerTile; ++pp) {
+        const int rp = __shfl_sync(0xffffffffu, rows, pp);
+        const int pg_id = __shfl_sync(0xffffffffu, page, pp);
+        if (lane == 0 && rp > 0) {
+          const int y = (pg_id * a.Hkv + g) * kPage;
+          const uint32_t sK = sST + uint32_t(s * L::STAGE), sV = sK + L::TILE;
+#pragma unroll
+          for (int cb = 0; cb < L::CB; ++cb) {
+            tma_load_2d(sK + uint32_t(cb * L::BLK + pp * kPage * 128), &tmk, cb * 64, y, BAR(B_KV_FULL + s));
+            tma_load_2d(sV + uint32_t(cb * L::BLK + pp * kPage * 128), &tmv, cb * 64, y, BAR(B_KV_FULL + s));
+          }
+        }
+      }
+      issued = j + 1;
+    }
+    // never leave copies in flight: wait (bounded) for the last loads of every stage
+    if (lane == 0) {
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        const uint32_t bar = BAR(B_KV_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else {
+    // ============================ MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t IQK = idesc_mma(kM, kN, 0, kQkF16 ? 1 : 0);
+      constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
+      const uint32_t tS = tmem, tO = tmem + 2 * kN;
+      bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
+      auto issue_pv = [&](int jj) -> bool {
+        if (!wait_bar(BAR(B_P_FULL), uint32_t(jj & 1), abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t sV = sST + uint32_t((jj % kStages) * L::STAGE) + L::TILE;
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          const uint64_t ad = sdesc(sP + uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32), 16, 1024);
+          const uint64_t bd = sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024);
+          mma_bf16(tO, ad, bd, IPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(BAR(B_PV_DONE));
+        mma_commit(BAR(B_KV_FREE + jj % kStages));
+        return true;
+      };
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int s = j % kStages, sbuf = j & 1;
+        if (!wait_bar(BAR(B_K_READY + s), uint32_t((j / kStages) & 1), abort_flag, a.status)) { ok = false; break; }
+        if (j >= 2 && !wait_bar(BAR(B_S_FREE + sbuf), uint32_t(((j >> 1) - 1) & 1), abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sK = sST + uint32_t(s * L::STAGE);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
+          mma_bf16(tS + uint32_t(sbuf * kN), sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), IQK,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(BAR(B_S_FULL + sbuf));
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(ntiles - 1);
+      // every MMA must be complete before TMEM is released
+      mma_commit(BAR(B_FINAL));
+      const uint64_t t0 = global_ns();
+      while (!mbar_test(BAR(B_FINAL), 0) && global_ns() - t0 < kWaitNs) {
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+  }
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Tensor map of a paged cache viewed as rows = num_pages * Hkv * 16, columns = D (bf16); one
+// TMA box = 16 rows (one page of one head) x 64 columns, 128-byte swizzle.
+static int cache_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int D) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return fail(LAZY_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(num_pages) * cuuint64_t(Hkv) * kPage};
+  const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
+  const cuuint32_t box[2] = {64, kPage};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LAZY_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+  return LAZY_OK;
+}
+
+template <int D, int POS>
+static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q, cudaStream_t st) {
+  using L = tc::Layout<D>;
+  auto kern = tc::prefill_tc_kernel<D, POS>;
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr[dev & 63]) {
+    LAZY_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM));
+    attr[dev & 63] = true;
+  }
+  const int G = a.Hq / a.Hkv;
+  const int tpt = tc::kM / G;
+  dim3 grid((max_q + tpt - 1) / tpt, a.Hkv, a.B);
+  kern<<<grid, tc::kThreads, L::SMEM, st>>>(mk, mv, a);
+  LAZY_CUDA_TRY(cudaGetLastError());
+  return LAZY_OK;
+}
+
+int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
+                   const uint64_t* meta, int B, int max_blocks, int max_q, const void* k_cache,
+                   const void* v_cache, int num_pages, int Hq, int Hkv, int D, const PosParams& pos, void* out,
+                   float* lse, cudaStream_t st) {
+  const int G = Hq / Hkv;
+  if (G > tc::kM || (tc::kM % G) != 0) return fail(LAZY_EINVAL, "Hq/Hkv = %d must divide 128", G);
+  CUtensorMap mk, mv;
+  int rc = cache_map(&mk, k_cache, num_pages, Hkv, D);
+  if (rc) return rc;
+  rc = cache_map(&mv, v_cache, num_pages, Hkv, D);
+  if (rc) return rc;
+  tc::Args a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.cu_q = cu_q;
+  a.q_start = q_start;
+  a.doc_blocks = doc_blocks;
+  a.meta = meta;
+  a.B = B;
+  a.max_blocks = max_blocks;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.num_pages = num_pages;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = status_word();
+  a.pos = pos;
+  const int kind = (pos.kind == kYarn) ? kRope : pos.kind;
+  if (D == 128) {
+    if (kind == kRope) return launch_tc<128, kRope>(mk, mv, a, max_q, st);
+    if (kind == kAlibi) return launch_tc<128, kAlibi>(mk, mv, a, max_q, st);
+    return launch_tc<128, kNone>(mk, mv, a, max_q, st);
+  }
+  if (kind == kRope) return launch_tc<64, kRope>(mk, mv, a, max_q, st);
+  if (kind == kAlibi) return launch_tc<64, kAlibi>(mk, mv, a, max_q, st);
+  return launch_tc<64, kNone>(mk, mv, a, max_q, st);
+}
+
+}  // namespace lazykv
