@@ -12,8 +12,10 @@
 //              write the 128B-swizzled K-major operand), then for every K tile: rotate each
 //              page's 16 rows by that page's Delta in place, in shared memory, and zero the V
 //              rows that hold no key (so no stale bits reach the tensor core).
-//   warp 8     producer: unpacks the 64-bit block words of the tile's 8 pages and issues TMA
-//              tile loads (box 16 rows x 64 columns, 128-byte swizzle) into a 2-stage ring.
+//   warp 8     producer: unpacks the 64-bit block words of the tile's 8 pages (prefetched one
+//              tile ahead) and issues TMA tile loads (box 16 rows x 64 columns, 128-byte
+//              swizzle) into separate 2-stage K and V rings: a K stage is refilled as soon as
+//              its QK^T has finished, a V stage once its PV has finished.
 //   warp 9     TMEM owner and MMA issuer: S = Q K^T (M 128, N 128, K 16 steps) into one of two
 //              TMEM S buffers, then O += P V (P from shared memory, V as an MN-major operand)
 //              into a TMEM accumulator; completion is signalled by tcgen05.commit.
@@ -34,7 +36,8 @@ namespace tc {
 constexpr int kM = 128;            // query rows per CTA
 constexpr int kN = 128;            // keys per K/V tile
 constexpr int kPagesPerTile = kN / kPage;
-constexpr int kStages = 2;
+constexpr int kStages = 2;       // K ring and V ring depth
+constexpr int kSlots = 4;        // per-tile metadata slots (tile j uses slot j % 4)
 constexpr int kThreads = 320;
 constexpr int kProdWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -42,16 +45,20 @@ constexpr float kTau = 8.0f;
 
 // barrier indices
 enum : int {
-  B_KV_FULL = 0,   // [2] TMA bytes landed
-  B_K_READY = 2,   // [2] K rotated, V cleaned (128 arrivals)
-  B_KV_FREE = 4,   // [2] stage consumed by QK and PV (commit)
-  B_S_FULL = 6,    // [2] S buffer written (commit)
-  B_S_FREE = 8,    // [2] S buffer read (128 arrivals)
-  B_P_FULL = 10,   // P tile written (128 arrivals)
-  B_PV_DONE = 11,  // PV finished (commit)
-  B_Q_READY = 12,  // Q tile prepared (128 arrivals)
-  B_FINAL = 13,    // all MMAs finished (commit)
-  NBAR = 14
+  B_K_FULL = 0,    // [2] K tile landed (TMA bytes)
+  B_K_READY = 2,   // [2] K tile rotated (128 arrivals)
+  B_K_FREE = 4,    // [2] QK^T done with the K stage (commit)
+  B_V_FULL = 6,    // [2] V tile landed (TMA bytes)
+  B_V_READY = 8,   // [2] key-less V rows cleared (128 arrivals); only tiles that need it
+                   //     complete a phase, so both sides count such tiles per stage
+  B_V_FREE = 10,   // [2] PV done with the V stage (commit)
+  B_S_FULL = 12,   // [2] S buffer written (commit)
+  B_S_FREE = 14,   // [2] S buffer read (128 arrivals)
+  B_P_FULL = 16,   // P tile written (128 arrivals)
+  B_PV_DONE = 17,  // PV finished (commit)
+  B_Q_READY = 18,  // Q tile prepared (128 arrivals)
+  B_FINAL = 19,    // all MMAs finished (commit)
+  NBAR = 20
 };
 
 template <int D>
@@ -61,12 +68,14 @@ struct Layout {
   static constexpr int TILE = kN * D * 2;                  // one K or V tile
   static constexpr int Q_OFF = 0;
   static constexpr int P_OFF = Q_OFF + kM * D * 2;
-  static constexpr int ST_OFF = P_OFF + kM * kN * 2;
-  static constexpr int STAGE = 2 * TILE;
-  static constexpr int KPOS_OFF = ST_OFF + kStages * STAGE;            // int [stage][128]
-  static constexpr int PINFO_OFF = KPOS_OFF + kStages * kN * 4;         // int2 [stage][8]
-  static constexpr int FLAG_OFF = PINFO_OFF + kStages * kPagesPerTile * 8;
-  static constexpr int CS_OFF = FLAG_OFF + 16;                          // float2 [8][D/2]
+  static constexpr int K_OFF = P_OFF + kM * kN * 2;        // K ring
+  static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
+  static constexpr int KPOS_OFF = V_OFF + kStages * TILE;  // int [slot][128] key positions
+  static constexpr int PINFO_OFF = KPOS_OFF + kSlots * kN * 4;          // int2 [slot][8] {Delta, rows}
+  static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, clean}
+  static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] physical pages
+  static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
+  static constexpr int CS_OFF = TURNS_OFF + (D / 2) * 8;                // float2 [8][D/2]
   static constexpr int BAR_OFF = CS_OFF + kPagesPerTile * (D / 2) * 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;                   // tmem slot, abort flag
   static constexpr int SMEM = MISC_OFF + 16 + 1024;                     // + alignment slack
@@ -189,6 +198,12 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ uint32_t swz(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 // ---------------------------------------------------------------- the kernel
+__device__ __forceinline__ float ex2(float x) {  // 2^x on the MUFU (approx, flush-to-zero)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D, int POS>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
@@ -220,10 +235,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
   const int ntiles = (nb + kPagesPerTile - 1) / kPagesPerTile;
 
-  const uint32_t sQ = sb + L::Q_OFF, sP = sb + L::P_OFF, sST = sb + L::ST_OFF;
+  const uint32_t sQ = sb + L::Q_OFF, sP = sb + L::P_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
   int* kpos = reinterpret_cast<int*>(sm + L::KPOS_OFF);
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
+  unsigned long long* turns = reinterpret_cast<unsigned long long*>(sm + L::TURNS_OFF);
   float2* cs = reinterpret_cast<float2*>(sm + L::CS_OFF);
   const uint32_t bar0 = sb + L::BAR_OFF;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
@@ -232,9 +248,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(BAR(B_KV_FULL + s), 1);
+      mbar_init(BAR(B_K_FULL + s), 1);
       mbar_init(BAR(B_K_READY + s), 128);
-      mbar_init(BAR(B_KV_FREE + s), 1);
+      mbar_init(BAR(B_K_FREE + s), 1);
+      mbar_init(BAR(B_V_FULL + s), 1);
+      mbar_init(BAR(B_V_READY + s), 128);
+      mbar_init(BAR(B_V_FREE + s), 1);
       mbar_init(BAR(B_S_FULL + s), 1);
       mbar_init(BAR(B_S_FREE + s), 128);
     }
@@ -245,6 +264,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if constexpr (kRotate)
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) turns[i] = a.pos.turns[i];
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot))
                  : "memory");
@@ -267,34 +288,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const uint32_t tl = tmem + (uint32_t(32 * warp) << 16);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int s = j % kStages, sbuf = j & 1;
+    for (int j = 0; j < ntiles; ++j) {
+      const int sbuf = j & 1, slot = j % kSlots;
       const bool got_s = wait_bar(BAR(B_S_FULL + sbuf), uint32_t((j >> 1) & 1), abort_flag, a.status);
       if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
       tc_fence_after();
-      const bool fast = (POS != kAlibi) && flags[s];
-      const int* kp = kpos + s * kN;
+      const bool fast = (POS != kAlibi) && flags[slot * 2];
+      const int* kp = kpos + slot * kN;
       float mx = -INFINITY;
 #pragma unroll
       for (int c4 = 0; c4 < kN / 32; ++c4) {
         uint32_t v[32];
         tmem_ld32(tl + uint32_t(sbuf * kN + c4 * 32), v);
         tmem_wait_ld();
+        if (fast) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(v[e]);
-          if (!fast) {
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float x = __uint_as_float(v[e]);
             const int p = kp[c4 * 32 + e];
             if constexpr (POS == kAlibi) x += slope * float(p - m_row);
-            x = (p <= m_row) ? x : -INFINITY;
+            mx = fmaxf(mx, (p <= m_row) ? x : -INFINITY);
           }
-          mx = fmaxf(mx, x);
         }
       }
       const bool need = mx > m_run + kTau;
       const float m_new = need ? mx : m_run;
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
+      const float2 mneg = make_float2(-m_use, -m_use);
       uint32_t pk[kN / 2];
-      float sum = 0.f;
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < kN / 32; ++c4) {
         uint32_t v[32];
@@ -302,22 +327,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float x0 = __uint_as_float(v[e]), x1 = __uint_as_float(v[e + 1]);
+          float2 x = make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
           if (!fast) {
             const int p0 = kp[c4 * 32 + e], p1 = kp[c4 * 32 + e + 1];
             if constexpr (POS == kAlibi) {
-              x0 += slope * float(p0 - m_row);
-              x1 += slope * float(p1 - m_row);
+              x.x += slope * float(p0 - m_row);
+              x.y += slope * float(p1 - m_row);
             }
-            x0 = (p0 <= m_row) ? x0 : -INFINITY;
-            x1 = (p1 <= m_row) ? x1 : -INFINITY;
+            x.x = (p0 <= m_row) ? x.x : -INFINITY;
+            x.y = (p1 <= m_row) ? x.y : -INFINITY;
           }
-          const float e0 = (m_new == -INFINITY) ? 0.f : exp2f(x0 - m_new);
-          const float e1 = (m_new == -INFINITY) ? 0.f : exp2f(x1 - m_new);
-          sum += e0 + e1;
-          pk[c4 * 16 + e / 2] = f2_to_bf2(e0, e1);
+          x = __fadd2_rn(x, mneg);
+          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+          sum2 = __fadd2_rn(sum2, ev);
+          pk[c4 * 16 + e / 2] = f2_to_bf2(ev.x, ev.y);
         }
       }
+      const float sum = sum2.x + sum2.y;
       tc_fence_before();
       mbar_arrive(BAR(B_S_FREE + sbuf));
       if (j > 0) {
@@ -325,7 +351,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (!__all_sync(0xffffffffu, got_pv)) { ok = false; break; }
         tc_fence_after();
       }
-      const float alpha = (j > 0 && need && m_run != -INFINITY) ? exp2f(m_run - m_new) : 1.f;
+      const float alpha = (j > 0 && need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
       l_run = (j == 0) ? sum : l_run * alpha + sum;
       if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
 #pragma unroll 1
@@ -402,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
               co = a.pos.table[(size_t)m * D + i];
               sn = a.pos.table[(size_t)m * D + D / 2 + i];
             } else {
-              turn_sincos(m, a.pos.turns[i], sn, co);
+              turn_sincos(m, turns[i], sn, co);
             }
             const float x1 = x[i], x2 = x[i + D / 2];
             x[i] = x1 * co - x2 * sn;
@@ -434,16 +460,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
     bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
+    int cleaned[kStages] = {0, 0};  // V_READY phases completed per stage
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kStages;
-      if (ok) ok = wait_bar(BAR(B_KV_FULL + s), uint32_t((j / kStages) & 1), abort_flag, a.status);
-      const int2 pi = ok ? pinfo[s * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, rows}
-      const uint32_t sK = sST + uint32_t(s * L::STAGE), sV = sK + L::TILE;
+      const int s = j % kStages, slot = j % kSlots;
+      const uint32_t par = uint32_t((j / kStages) & 1);
+      if (ok) ok = wait_bar(BAR(B_K_FULL + s), par, abort_flag, a.status);
+      const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, rows}
       if constexpr (kRotate) {
+        const uint32_t sK = sK0 + uint32_t(s * L::TILE);
         for (int idx = rt; ok && idx < kPagesPerTile * (D / 2); idx += 128) {
           const int pp = idx / (D / 2), i = idx % (D / 2);
           float sn, co;
-          turn_sincos(uint32_t(pinfo[s * kPagesPerTile + pp].x), a.pos.turns[i], sn, co);
+          turn_sincos(uint32_t(pinfo[slot * kPagesPerTile + pp].x), turns[i], sn, co);
           cs[idx] = make_float2(co, sn);
         }
         named_sync(1, 128);
@@ -469,31 +497,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             st_shared_v4(a2, u2);
           }
         }
+        fence_async_smem();
+        named_sync(1, 128);  // cos/sin table reused next tile
       }
-      if (ok && t >= pi.y) {  // no key in this row: clear V so no stale bits reach the MMA
-#pragma unroll
-        for (int cb = 0; cb < L::CB; ++cb)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(rt, c), make_uint4(0, 0, 0, 0));
-      }
-      fence_async_smem();
-      if constexpr (kRotate) named_sync(1, 128);  // cos/sin table reused next tile
+      // V: rows holding no key are cleared so no stale bits reach the tensor core.  Waiting for
+      // this tile's V also means the previous PV on this stage is done, so V_READY can never run
+      // two phases ahead of the MMA thread.
+      const bool clean = flags[slot * 2 + 1] != 0;
       mbar_arrive(BAR(B_K_READY + s));
+      if (clean) {
+        if (ok) ok = wait_bar(BAR(B_V_FULL + s), par, abort_flag, a.status);
+        if (ok && t >= pi.y) {
+          const uint32_t sV = sV0 + uint32_t(s * L::TILE);
+#pragma unroll
+          for (int cb = 0; cb < L::CB; ++cb)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(rt, c), make_uint4(0, 0, 0, 0));
+        }
+        fence_async_smem();
+        mbar_arrive(BAR(B_V_READY + s));
+        ++cleaned[s];
+      }
     }
   } else if (warp == kProdWarp) {
     // ============================ block words + TMA
+    // Issue order K0, K1, V0, K2, V1, ...: a K stage is refilled once its QK^T is done, a V
+    // stage once its PV is done, and no K load waits behind an earlier tile's PV.
     const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
-    int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kStages;
-      if (j >= kStages) {
-        const bool freed = wait_bar(BAR(B_KV_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, freed)) break;
-      }
+    int* pgid = reinterpret_cast<int*>(sm + L::PGID_OFF);
+    auto fetch = [&](int j) -> uint64_t {  // lane < 8: block word of page slot `lane` of tile j
+      const int jb = j * kPagesPerTile + lane;
+      return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
+    };
+    uint64_t w_next = fetch(0);
+    int issued_k = 0, issued_v = 0;
+    // K of tile j: wait for its stage, publish the tile's metadata, load the pages
+    auto issue_k = [&](int j) -> bool {
+      const int s = j % kStages, slot = j % kSlots;
+      const uint64_t w = w_next;
+      w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
       int rows = 0, start = 0, page = 0, delta = 0;
       const int jb = j * kPagesPerTile + lane;
       if (lane < kPagesPerTile && jb < nb) {
-        const uint64_t w = ldg_u64(mrow + jb);
         page = int(word_page(w));
         delta = int(word_delta(w));
         start = delta + kPage * int(word_pg(w));
@@ -503,41 +548,88 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           rows = 0;
         }
       }
-      if (lane < kPagesPerTile) pinfo[s * kPagesPerTile + lane] = make_int2(delta, rows);
+      if (j >= kStages) {
+        const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, freed)) return false;
+      }
+      if (lane < kPagesPerTile) {
+        pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
+        pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int idx = lane * 4 + e, pp = idx >> 4, tt = idx & 15;
         const int rp = __shfl_sync(0xffffffffu, rows, pp);
         const int sp = __shfl_sync(0xffffffffu, start, pp);
-        kpos[s * kN + idx] = tt < rp ? sp + tt : INT_MAX;
+        kpos[slot * kN + idx] = tt < rp ? sp + tt : INT_MAX;
       }
       const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
       const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
-      if (lane == 0) flags[s] = all16 && (last_start + kPage - 1 <= m_min);
+      if (lane == 0) {
+        flags[slot * 2] = all16 && (last_start + kPage - 1 <= m_min);  // every key visible to every row
+        flags[slot * 2 + 1] = !all16;                                  // some V rows must be cleared
+      }
       __syncwarp();
       uint32_t bytes = 0;
       for (int pp = 0; pp < kPagesPerTile; ++pp)
-        if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += 2u * kPage * D * 2;
-      if (lane == 0) mbar_arrive_expect_tx(BAR(B_KV_FULL + s), bytes);
-      for (int pp = 0; pp < kPagesPerTile; ++pp) {
-        const int rp = __shfl_sync(0xffffffffu, rows, pp);
-        const int pg_id = __shfl_sync(0xffffffffu, page, pp);
-        if (lane == 0 && rp > 0) {
-          const int y = (pg_id * a.Hkv + g) * kPage;
-          const uint32_t sK = sST + uint32_t(s * L::STAGE), sV = sK + L::TILE;
+        if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += uint32_t(kPage) * D * 2;
+      const uint32_t sK = sK0 + uint32_t(s * L::TILE);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
+        for (int pp = 0; pp < kPagesPerTile; ++pp) {
+          const int pg_id = pgid[slot * kPagesPerTile + pp];
+          if (pg_id >= 0)
 #pragma unroll
-          for (int cb = 0; cb < L::CB; ++cb) {
-            tma_load_2d(sK + uint32_t(cb * L::BLK + pp * kPage * 128), &tmk, cb * 64, y, BAR(B_KV_FULL + s));
-            tma_load_2d(sV + uint32_t(cb * L::BLK + pp * kPage * 128), &tmv, cb * 64, y, BAR(B_KV_FULL + s));
-          }
+            for (int cb = 0; cb < L::CB; ++cb)
+              tma_load_2d(sK + uint32_t(cb * L::BLK + pp * kPage * 128), &tmk, cb * 64, (pg_id * a.Hkv + g) * kPage,
+                          BAR(B_K_FULL + s));
         }
       }
-      issued = j + 1;
+      __syncwarp();
+      issued_k = j + 1;
+      return true;
+    };
+    // V of tile j (its metadata was published with its K)
+    auto issue_v = [&](int j) -> bool {
+      const int s = j % kStages, slot = j % kSlots;
+      if (j >= kStages) {
+        const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, freed)) return false;
+      }
+      const uint32_t sV = sV0 + uint32_t(s * L::TILE);
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int pp = 0; pp < kPagesPerTile; ++pp)
+          if (pgid[slot * kPagesPerTile + pp] >= 0) bytes += uint32_t(kPage) * D * 2;
+        mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
+        for (int pp = 0; pp < kPagesPerTile; ++pp) {
+          const int pg_id = pgid[slot * kPagesPerTile + pp];
+          if (pg_id >= 0)
+#pragma unroll
+            for (int cb = 0; cb < L::CB; ++cb)
+              tma_load_2d(sV + uint32_t(cb * L::BLK + pp * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
+                          BAR(B_V_FULL + s));
+        }
+      }
+      __syncwarp();
+      issued_v = j + 1;
+      return true;
+    };
+    bool ok = issue_k(0);
+    for (int j = 0; j < ntiles && ok; ++j) {
+      if (j + 1 < ntiles) ok = issue_k(j + 1);
+      if (ok) ok = issue_v(j);
     }
     // never leave copies in flight: wait (bounded) for the last loads of every stage
     if (lane == 0) {
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
-        const uint32_t bar = BAR(B_KV_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+      for (int j = max(0, issued_k - kStages); j < issued_k; ++j) {
+        const uint32_t bar = BAR(B_K_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+        }
+      }
+      for (int j = max(0, issued_v - kStages); j < issued_v; ++j) {
+        const uint32_t bar = BAR(B_V_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
         const uint64_t t0 = global_ns();
         while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
         }
@@ -550,10 +642,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
       const uint32_t tS = tmem, tO = tmem + 2 * kN;
       bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
-      auto issue_pv = [&](int jj) -> bool {
+      int cleaned[kStages] = {0, 0};  // V_READY phases consumed per stage
+      bool clean_prev = false;        // clean flag of the tile whose PV is issued next
+      auto issue_pv = [&](int jj, bool clean) -> bool {
+        const int s = jj % kStages;
+        const uint32_t par = uint32_t((jj / kStages) & 1);
         if (!wait_bar(BAR(B_P_FULL), uint32_t(jj & 1), abort_flag, a.status)) return false;
+        if (!wait_bar(BAR(B_V_FULL + s), par, abort_flag, a.status)) return false;
+        if (clean) {
+          if (!wait_bar(BAR(B_V_READY + s), uint32_t(cleaned[s] & 1), abort_flag, a.status)) return false;
+          ++cleaned[s];
+        }
         tc_fence_after();
-        const uint32_t sV = sST + uint32_t((jj % kStages) * L::STAGE) + L::TILE;
+        const uint32_t sV = sV0 + uint32_t(s * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < kN / 16; ++kk) {
           const uint64_t ad = sdesc(sP + uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32), 16, 1024);
@@ -561,7 +662,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           mma_bf16(tO, ad, bd, IPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(BAR(B_PV_DONE));
-        mma_commit(BAR(B_KV_FREE + jj % kStages));
+        mma_commit(BAR(B_V_FREE + s));
         return true;
       };
       for (int j = 0; j < ntiles && ok; ++j) {
@@ -572,7 +673,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           break;
         }
         tc_fence_after();
-        const uint32_t sK = sST + uint32_t(s * L::STAGE);
+        const bool clean_j = flags[(j % kSlots) * 2 + 1] != 0;  // published before K_FULL of tile j
+        const uint32_t sK = sK0 + uint32_t(s * L::TILE);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
@@ -580,9 +682,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(BAR(B_S_FULL + sbuf));
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+        mma_commit(BAR(B_K_FREE + s));
+        if (j >= 1 && !issue_pv(j - 1, clean_prev)) { ok = false; break; }
+        clean_prev = clean_j;
       }
-      if (ok) issue_pv(ntiles - 1);
+      if (ok) issue_pv(ntiles - 1, clean_prev);
       // every MMA must be complete before TMEM is released
       mma_commit(BAR(B_FINAL));
       const uint64_t t0 = global_ns();
