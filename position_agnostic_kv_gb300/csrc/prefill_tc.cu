@@ -240,7 +240,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
   unsigned long long* turns = reinterpret_cast<unsigned long long*>(sm + L::TURNS_OFF);
-  float2* cs = reinterpret_cast<float2*>(sm + L::CS_OFF);
+  float4* cs4 = reinterpret_cast<float4*>(sm + L::CS_OFF);
   const uint32_t bar0 = sb + L::BAR_OFF;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
@@ -295,57 +295,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       tc_fence_after();
       const bool fast = (POS != kAlibi) && flags[slot * 2];
       const int* kp = kpos + slot * kN;
-      float mx = -INFINITY;
+      // the whole S row in registers: four loads, one wait, then the buffer is released
+      uint32_t v[kN];
+      tmem_ld32(tl + uint32_t(sbuf * kN + 0), *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+      tmem_ld32(tl + uint32_t(sbuf * kN + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld32(tl + uint32_t(sbuf * kN + 64), *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld32(tl + uint32_t(sbuf * kN + 96), *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      tmem_wait_ld();
+      if (!fast) {  // mask (and ALiBi) before S is released: releasing it lets slot j % 4 be reused
 #pragma unroll
-      for (int c4 = 0; c4 < kN / 32; ++c4) {
-        uint32_t v[32];
-        tmem_ld32(tl + uint32_t(sbuf * kN + c4 * 32), v);
-        tmem_wait_ld();
-        if (fast) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float x = __uint_as_float(v[e]);
-            const int p = kp[c4 * 32 + e];
-            if constexpr (POS == kAlibi) x += slope * float(p - m_row);
-            mx = fmaxf(mx, (p <= m_row) ? x : -INFINITY);
-          }
+        for (int e = 0; e < kN; ++e) {
+          float x = __uint_as_float(v[e]);
+          const int p = kp[e];
+          if constexpr (POS == kAlibi) x += slope * float(p - m_row);
+          v[e] = __float_as_uint((p <= m_row) ? x : -INFINITY);
         }
       }
+      tc_fence_before();
+      mbar_arrive(BAR(B_S_FREE + sbuf));
+      float mx = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < kN; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
       const bool need = mx > m_run + kTau;
       const float m_new = need ? mx : m_run;
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
       const float2 mneg = make_float2(-m_use, -m_use);
-      uint32_t pk[kN / 2];
       float2 sum2 = make_float2(0.f, 0.f);
+      // P packed to bf16 pairs in place: pair e lands in v[e] (already consumed)
 #pragma unroll
-      for (int c4 = 0; c4 < kN / 32; ++c4) {
-        uint32_t v[32];
-        tmem_ld32(tl + uint32_t(sbuf * kN + c4 * 32), v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 x = make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          if (!fast) {
-            const int p0 = kp[c4 * 32 + e], p1 = kp[c4 * 32 + e + 1];
-            if constexpr (POS == kAlibi) {
-              x.x += slope * float(p0 - m_row);
-              x.y += slope * float(p1 - m_row);
-            }
-            x.x = (p0 <= m_row) ? x.x : -INFINITY;
-            x.y = (p1 <= m_row) ? x.y : -INFINITY;
-          }
-          x = __fadd2_rn(x, mneg);
-          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
-          sum2 = __fadd2_rn(sum2, ev);
-          pk[c4 * 16 + e / 2] = f2_to_bf2(ev.x, ev.y);
-        }
+      for (int e = 0; e < kN / 2; ++e) {
+        float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        x = __fadd2_rn(x, mneg);
+        const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+        sum2 = __fadd2_rn(sum2, ev);
+        v[e] = f2_to_bf2(ev.x, ev.y);
       }
       const float sum = sum2.x + sum2.y;
-      tc_fence_before();
-      mbar_arrive(BAR(B_S_FREE + sbuf));
+      uint32_t* pk = v;
       if (j > 0) {
         const bool got_pv = wait_bar(BAR(B_PV_DONE), uint32_t((j - 1) & 1), abort_flag, a.status);
         if (!__all_sync(0xffffffffu, got_pv)) { ok = false; break; }
@@ -468,15 +454,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, rows}
       if constexpr (kRotate) {
         const uint32_t sK = sK0 + uint32_t(s * L::TILE);
-        for (int idx = rt; ok && idx < kPagesPerTile * (D / 2); idx += 128) {
-          const int pp = idx / (D / 2), i = idx % (D / 2);
-          float sn, co;
-          turn_sincos(uint32_t(pinfo[slot * kPagesPerTile + pp].x), turns[i], sn, co);
-          cs[idx] = make_float2(co, sn);
+        // cos/sin rows only for pages that start a new document offset: page pp uses the row of
+        // the first page of its run of equal Delta (consecutive pages of a document share it)
+        int run_start = 0;
+        if (ok) {
+#pragma unroll
+          for (int pp = 1; pp <= ps; ++pp)
+            if (pinfo[slot * kPagesPerTile + pp].x != pinfo[slot * kPagesPerTile + pp - 1].x) run_start = pp;
+        }
+        for (int idx = rt; ok && idx < kPagesPerTile * (D / 4); idx += 128) {
+          const int pp = idx / (D / 4), q = idx % (D / 4);
+          const int dl = pinfo[slot * kPagesPerTile + pp].x;
+          if (pp == 0 || dl != pinfo[slot * kPagesPerTile + pp - 1].x) {
+            float s0, c0, s1, c1;
+            turn_sincos(uint32_t(dl), turns[2 * q], s0, c0);
+            turn_sincos(uint32_t(dl), turns[2 * q + 1], s1, c1);
+            cs4[idx] = make_float4(c0, c1, s0, s1);
+          }
         }
         named_sync(1, 128);
         if (ok && t < pi.y) {
-          const float2* c2 = cs + ps * (D / 2);
+          const float4* c4 = cs4 + run_start * (D / 4);
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             // pair i = c*8 + e: element i and its partner i + D/2 share the swizzled chunk slot
@@ -487,11 +485,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              const float2 cA = c2[c * 8 + 2 * w], cB = c2[c * 8 + 2 * w + 1];
-              const float x1a = bf_lo(p1[w]), x1b = bf_hi(p1[w]);
-              const float x2a = bf_lo(p2[w]), x2b = bf_hi(p2[w]);
-              p1[w] = f2_to_h2(x1a * cA.x - x2a * cA.y, x1b * cB.x - x2b * cB.y);
-              p2[w] = f2_to_h2(x1a * cA.y + x2a * cA.x, x1b * cB.y + x2b * cB.x);
+              const float4 cc = c4[c * 4 + w];  // pairs c*8 + 2w, c*8 + 2w + 1
+              const float2 cv = make_float2(cc.x, cc.y), sv = make_float2(cc.z, cc.w);
+              const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
+              const float2 t1 = __fmul2_rn(x2, sv), t2 = __fmul2_rn(x2, cv);
+              const float2 y1 = __ffma2_rn(x1, cv, make_float2(-t1.x, -t1.y));  // x1 c - x2 s
+              const float2 y2 = __ffma2_rn(x1, sv, t2);                          // x1 s + x2 c
+              p1[w] = f2_to_h2(y1.x, y1.y);
+              p2[w] = f2_to_h2(y2.x, y2.y);
             }
             st_shared_v4(a1, u1);
             st_shared_v4(a2, u2);
@@ -500,11 +501,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         fence_async_smem();
         named_sync(1, 128);  // cos/sin table reused next tile
       }
+      mbar_arrive(BAR(B_K_READY + s));
       // V: rows holding no key are cleared so no stale bits reach the tensor core.  Waiting for
       // this tile's V also means the previous PV on this stage is done, so V_READY can never run
       // two phases ahead of the MMA thread.
       const bool clean = flags[slot * 2 + 1] != 0;
-      mbar_arrive(BAR(B_K_READY + s));
       if (clean) {
         if (ok) ok = wait_bar(BAR(B_V_FULL + s), par, abort_flag, a.status);
         if (ok && t >= pi.y) {
@@ -574,17 +575,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       for (int pp = 0; pp < kPagesPerTile; ++pp)
         if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += uint32_t(kPage) * D * 2;
       const uint32_t sK = sK0 + uint32_t(s * L::TILE);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
-        for (int pp = 0; pp < kPagesPerTile; ++pp) {
-          const int pg_id = pgid[slot * kPagesPerTile + pp];
-          if (pg_id >= 0)
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
+      __syncwarp();
+      if (lane < kPagesPerTile && rows > 0)  // one lane per page: TMA issue is per-instruction bound
 #pragma unroll
-            for (int cb = 0; cb < L::CB; ++cb)
-              tma_load_2d(sK + uint32_t(cb * L::BLK + pp * kPage * 128), &tmk, cb * 64, (pg_id * a.Hkv + g) * kPage,
-                          BAR(B_K_FULL + s));
-        }
-      }
+        for (int cb = 0; cb < L::CB; ++cb)
+          tma_load_2d(sK + uint32_t(cb * L::BLK + lane * kPage * 128), &tmk, cb * 64, (page * a.Hkv + g) * kPage,
+                      BAR(B_K_FULL + s));
       __syncwarp();
       issued_k = j + 1;
       return true;
@@ -597,20 +594,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (!__all_sync(0xffffffffu, freed)) return false;
       }
       const uint32_t sV = sV0 + uint32_t(s * L::TILE);
-      if (lane == 0) {
-        uint32_t bytes = 0;
-        for (int pp = 0; pp < kPagesPerTile; ++pp)
-          if (pgid[slot * kPagesPerTile + pp] >= 0) bytes += uint32_t(kPage) * D * 2;
-        mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
-        for (int pp = 0; pp < kPagesPerTile; ++pp) {
-          const int pg_id = pgid[slot * kPagesPerTile + pp];
-          if (pg_id >= 0)
+      const int pg_id = lane < kPagesPerTile ? pgid[slot * kPagesPerTile + lane] : -1;
+      const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, pg_id >= 0))) * kPage * D * 2;
+      if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
+      __syncwarp();
+      if (pg_id >= 0)
 #pragma unroll
-            for (int cb = 0; cb < L::CB; ++cb)
-              tma_load_2d(sV + uint32_t(cb * L::BLK + pp * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
-                          BAR(B_V_FULL + s));
-        }
-      }
+        for (int cb = 0; cb < L::CB; ++cb)
+          tma_load_2d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
+                      BAR(B_V_FULL + s));
       __syncwarp();
       issued_v = j + 1;
       return true;
