@@ -444,12 +444,14 @@ int decode_group(int Hq, int Hkv) {
 }
 
 int choose_splits(int rows, int Hq, int Hkv, int max_blocks) {
-  const int groups = Hq / decode_group(Hq, Hkv);
-  const long long units = (long long)rows * groups;
-  const int sms = sm_count();
-  // at least ~8 CTA waves (2 CTAs per SM) over the GPU, at least 8 pages per warp
-  const long long want = (8LL * sms * 2 + units - 1) / units;
-  const int max_by_len = max(1, max_blocks / (kDecWarps * 8));
+  const int G = decode_group(Hq, Hkv);
+  const long long units = (long long)rows * (Hq / G);
+  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // CTAs resident at once
+  // About 4 waves of resident CTAs, but at least 16 pages per warp: measured on GB300, long
+  // per-warp page runs beat more, shorter CTAs (every CTA pays a pipeline start-up and its
+  // split partials), and a partial last wave costs little once there are several waves.
+  const long long want = (4 * slots + units - 1) / units;
+  const int max_by_len = max(1, max_blocks / (kDecWarps * 16));
   long long s = want < max_by_len ? want : max_by_len;
   if (s < 1) s = 1;
   if (s > 64) s = 64;
