@@ -6,22 +6,29 @@
 // the K tile is split in its two half-dimensions, rotated, then multiplied.  [GIST]
 // Prefilling: a single relative rotation by the offset, never un-rotate then re-rotate.
 //
-// GB300 design (one CTA per (request, KV head, 128 query rows); 320 threads, 1 CTA per SM):
-//   warps 0-3  softmax + epilogue.  Thread r owns TMEM lane r = query row r of the tile.
-//   warps 4-7  Q preparation (rotate by its absolute position m, fold in the softmax scale,
-//              write the 128B-swizzled K-major operand), then for every K tile: rotate each
-//              page's 16 rows by that page's Delta in place, in shared memory, and zero the V
-//              rows that hold no key (so no stale bits reach the tensor core).
-//   warp 8     producer: unpacks the 64-bit block words of the tile's 8 pages (prefetched one
-//              tile ahead) and issues TMA tile loads (box 16 rows x 64 columns, 128-byte
-//              swizzle) into separate 2-stage K and V rings: a K stage is refilled as soon as
-//              its QK^T has finished, a V stage once its PV has finished.
-//   warp 9     TMEM owner and MMA issuer: S = Q K^T (M 128, N 128, K 16 steps) into one of two
-//              TMEM S buffers, then O += P V (P from shared memory, V as an MN-major operand)
-//              into a TMEM accumulator; completion is signalled by tcgen05.commit.
-// GQA: the tile's rows are (token, head) pairs of the KV head's query-head group, token-major,
-// so one K/V tile serves G heads.  Online softmax in base 2; the running max moves (and O is
-// rescaled in TMEM) only when a row's max grows by more than 8.  Every wait is bounded.
+// GB300 design.  One CTA per (request, KV head, 256 query rows) = two 128-row Q tiles that share
+// every K/V tile, so each staged (and rotated) K tile and each V tile feeds twice the MMA work.
+// 512 threads, 1 CTA per SM, registers re-split per warpgroup with setmaxnreg:
+//   warps 0-3 / 4-7  softmax of Q tile 0 / 1 (thread r owns TMEM lane r = row r of its tile):
+//              prepare the tile's Q rows (rotation by the absolute position m, softmax scale
+//              folded in, 128B-swizzled K-major operand), then per K tile: S row from TMEM, mask,
+//              online softmax in base 2 (the running max moves, and O is rescaled in TMEM, only
+//              when a row's max grows by more than 8), P written back to TMEM over S as bf16.
+//   warps 8-11 K rotation: each staged K tile's page rows rotated by their page's Delta in
+//              place in shared memory (cos/sin only per distinct Delta); V rows that hold no key
+//              are zeroed so no stale bits reach the tensor core.
+//   warp 12    producer: unpacks the 64-bit block words of a tile's 8 pages (prefetched one tile
+//              ahead) and issues TMA loads (box 16 rows x 64 columns, 128-byte swizzle) into
+//              2-stage K and V rings.
+//   warp 13    TMEM owner and MMA issuer, in the order QK0(j) QK1(j) | PV0(j) QK0(j+1) PV1(j)
+//              QK1(j+1) | ...: S_i = Q_i K^T (A and B from shared memory) into TMEM, then
+//              O_i += P_i V with P_i read from TMEM (A operand in tensor memory) and V as an
+//              MN-major shared-memory operand.  The tensor pipe runs a thread's MMAs in issue
+//              order, so S_i of tile j+1 is only written after PV_i(j) has read P_i, and the
+//              commit that signals S_i(j+1) also covers PV_i(j).
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64 of S_i.
+// GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
+// Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
 #include <cfloat>
 #include <climits>
 
@@ -33,32 +40,40 @@ namespace lazykv {
 
 namespace tc {
 
-constexpr int kM = 128;            // query rows per CTA
+constexpr int kM = 128;            // query rows per Q tile
+constexpr int kQT = 2;             // Q tiles per CTA
 constexpr int kN = 128;            // keys per K/V tile
 constexpr int kPagesPerTile = kN / kPage;
-constexpr int kStages = 2;       // K ring and V ring depth
-constexpr int kSlots = 4;        // per-tile metadata slots (tile j uses slot j % 4)
-constexpr int kThreads = 320;
-constexpr int kProdWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kStages = 2;         // K ring and V ring depth
+constexpr int kSlots = 4;          // per-tile metadata slots (tile j uses slot j % 4)
+constexpr int kThreads = 512;
+constexpr int kRotWarp0 = 8;
+constexpr int kProdWarp = 12;
+constexpr int kMmaWarp = 13;
+// registers per thread after the re-split (no spills at this split):
+// 2*128*184 + 128*56 + 128*88 = 65536 = 512 * 128
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsSoftmax = 184;
+constexpr int kRegsRot = 56;
+constexpr int kRegsIssue = 88;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsRot + 128 * kRegsIssue == kThreads * kRegsLaunch,
+              "warpgroup register shares must add up to the launch allocation");
 constexpr float kTau = 8.0f;
 
 // barrier indices
 enum : int {
   B_K_FULL = 0,    // [2] K tile landed (TMA bytes)
   B_K_READY = 2,   // [2] K tile rotated (128 arrivals)
-  B_K_FREE = 4,    // [2] QK^T done with the K stage (commit)
+  B_K_FREE = 4,    // [2] both QK^T done with the K stage (commit)
   B_V_FULL = 6,    // [2] V tile landed (TMA bytes)
   B_V_READY = 8,   // [2] key-less V rows cleared (128 arrivals); only tiles that need it
                    //     complete a phase, so both sides count such tiles per stage
-  B_V_FREE = 10,   // [2] PV done with the V stage (commit)
-  B_S_FULL = 12,   // [2] S buffer written (commit)
-  B_S_FREE = 14,   // [2] S buffer read (128 arrivals)
-  B_P_FULL = 16,   // P tile written (128 arrivals)
-  B_PV_DONE = 17,  // PV finished (commit)
-  B_Q_READY = 18,  // Q tile prepared (128 arrivals)
-  B_FINAL = 19,    // all MMAs finished (commit)
-  NBAR = 20
+  B_V_FREE = 10,   // [2] both PV done with the V stage (commit)
+  B_S_FULL = 12,   // [2] per Q tile: S written (commit; also covers that tile's previous PV)
+  B_P_FULL = 14,   // [2] per Q tile: P written to TMEM, O rescaled (128 arrivals)
+  B_Q_READY = 16,  // both Q tiles prepared (256 arrivals)
+  B_FINAL = 17,    // all MMAs finished (commit)
+  NBAR = 18
 };
 
 template <int D>
@@ -66,9 +81,9 @@ struct Layout {
   static constexpr int CB = D / 64;                        // 128-byte column blocks per row
   static constexpr int BLK = kM * 128;                     // one column block of a 128-row tile
   static constexpr int TILE = kN * D * 2;                  // one K or V tile
+  static constexpr int QTILE = kM * D * 2;                 // one Q tile
   static constexpr int Q_OFF = 0;
-  static constexpr int P_OFF = Q_OFF + kM * D * 2;
-  static constexpr int K_OFF = P_OFF + kM * kN * 2;        // K ring
+  static constexpr int K_OFF = Q_OFF + kQT * QTILE;        // K ring
   static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
   static constexpr int KPOS_OFF = V_OFF + kStages * TILE;  // int [slot][128] key positions
   static constexpr int PINFO_OFF = KPOS_OFF + kSlots * kN * 4;          // int2 [slot][8] {Delta, rows}
@@ -80,6 +95,7 @@ struct Layout {
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;                   // tmem slot, abort flag
   static constexpr int SMEM = MISC_OFF + 16 + 1024;                     // + alignment slack
 };
+static_assert(Layout<128>::SMEM <= 227 * 1024, "shared memory budget");
 
 struct Args {
   const __nv_bfloat16* q;
@@ -197,6 +213,15 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 // byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled block (1024-byte atoms)
 __device__ __forceinline__ uint32_t swz(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
 
+// O += P V with P (the A operand, M x K, 16-bit pairs packed per 32-bit column) in TMEM
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- the kernel
 __device__ __forceinline__ float ex2(float x) {  // 2^x on the MUFU (approx, flush-to-zero)
   float y;
@@ -218,15 +243,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int mp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
-  const int tpt = kM / G;  // tokens per tile
+  const int tpt = kM / G;  // tokens per Q tile
   const int q0 = a.cu_q[b];
   const int Lq = a.cu_q[b + 1] - q0;
-  const int tok0 = mt * tpt;
+  const int tok0 = mp * kQT * tpt;
   if (tok0 >= Lq) return;  // uniform for the CTA, before any barrier or TMEM use
+  const int nq = (tok0 + tpt < Lq) ? 2 : 1;  // live Q tiles
   const int qs = a.q_start[b];
-  const int ntok = min(tpt, Lq - tok0);
+  const int ntok = min(kQT * tpt, Lq - tok0);
   const int m_min = qs + tok0, m_max = qs + tok0 + ntok - 1;
   int nb = a.doc_blocks[b] + (m_max - qs) / kPage + 1;
   if (nb > a.max_blocks) {
@@ -235,7 +261,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
   const int ntiles = (nb + kPagesPerTile - 1) / kPagesPerTile;
 
-  const uint32_t sQ = sb + L::Q_OFF, sP = sb + L::P_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
+  const uint32_t sQ0 = sb + L::Q_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
   int* kpos = reinterpret_cast<int*>(sm + L::KPOS_OFF);
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
@@ -254,12 +280,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       mbar_init(BAR(B_V_FULL + s), 1);
       mbar_init(BAR(B_V_READY + s), 128);
       mbar_init(BAR(B_V_FREE + s), 1);
-      mbar_init(BAR(B_S_FULL + s), 1);
-      mbar_init(BAR(B_S_FREE + s), 128);
     }
-    mbar_init(BAR(B_P_FULL), 128);
-    mbar_init(BAR(B_PV_DONE), 1);
-    mbar_init(BAR(B_Q_READY), 128);
+    for (int i = 0; i < kQT; ++i) {
+      mbar_init(BAR(B_S_FULL + i), 1);
+      mbar_init(BAR(B_P_FULL + i), 128);
+    }
+    mbar_init(BAR(B_Q_READY), 2 * 128);
     mbar_init(BAR(B_FINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -274,125 +300,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S0 at +0, S1 at +128, O at +256
+  const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
-    // ============================ softmax + epilogue (TMEM lanes 32*warp .. +32)
-    const int r = threadIdx.x;                 // query row of the tile
-    const int token = tok0 + r / G;
+  if (warp < 2 * 4) {
+    // ============================ Q preparation, softmax and epilogue of Q tile qt
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int qt = warp >> 2;
+    const int r = threadIdx.x & (kM - 1);  // row of the tile = TMEM lane
+    const int token = tok0 + qt * tpt + r / G;
     const int h = g * G + r % G;
     const bool valid = token < Lq;
     const int m_row = valid ? qs + token : -1;
-    float slope = 0.f;
-    if constexpr (POS == kAlibi) slope = a.pos.slopes[h] * 1.4426950408889634f;
-    const uint32_t tl = tmem + (uint32_t(32 * warp) << 16);
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int sbuf = j & 1, slot = j % kSlots;
-      const bool got_s = wait_bar(BAR(B_S_FULL + sbuf), uint32_t((j >> 1) & 1), abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
-      tc_fence_after();
-      const bool fast = (POS != kAlibi) && flags[slot * 2];
-      const int* kp = kpos + slot * kN;
-      // the whole S row in registers: four loads, one wait, then the buffer is released
-      uint32_t v[kN];
-      tmem_ld32(tl + uint32_t(sbuf * kN + 0), *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-      tmem_ld32(tl + uint32_t(sbuf * kN + 32), *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-      tmem_ld32(tl + uint32_t(sbuf * kN + 64), *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-      tmem_ld32(tl + uint32_t(sbuf * kN + 96), *reinterpret_cast<uint32_t(*)[32]>(v + 96));
-      tmem_wait_ld();
-      if (!fast) {  // mask (and ALiBi) before S is released: releasing it lets slot j % 4 be reused
-#pragma unroll
-        for (int e = 0; e < kN; ++e) {
-          float x = __uint_as_float(v[e]);
-          const int p = kp[e];
-          if constexpr (POS == kAlibi) x += slope * float(p - m_row);
-          v[e] = __float_as_uint((p <= m_row) ? x : -INFINITY);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(B_S_FREE + sbuf));
-      float mx = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < kN; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-      const bool need = mx > m_run + kTau;
-      const float m_new = need ? mx : m_run;
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
-      const float2 mneg = make_float2(-m_use, -m_use);
-      float2 sum2 = make_float2(0.f, 0.f);
-      // P packed to bf16 pairs in place: pair e lands in v[e] (already consumed)
-#pragma unroll
-      for (int e = 0; e < kN / 2; ++e) {
-        float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-        x = __fadd2_rn(x, mneg);
-        const float2 ev = make_float2(ex2(x.x), ex2(x.y));
-        sum2 = __fadd2_rn(sum2, ev);
-        v[e] = f2_to_bf2(ev.x, ev.y);
-      }
-      const float sum = sum2.x + sum2.y;
-      uint32_t* pk = v;
-      if (j > 0) {
-        const bool got_pv = wait_bar(BAR(B_PV_DONE), uint32_t((j - 1) & 1), abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, got_pv)) { ok = false; break; }
-        tc_fence_after();
-      }
-      const float alpha = (j > 0 && need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
-      l_run = (j == 0) ? sum : l_run * alpha + sum;
-      if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tl + uint32_t(2 * kN + c * 32), v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st32(tl + uint32_t(2 * kN + c * 32), v);
-        }
-        tmem_wait_st();
-      }
-      m_run = m_new;
-      // P row -> shared memory, K-major, 128-byte swizzle (2 column blocks of 64 keys)
-#pragma unroll
-      for (int cb = 0; cb < kN / 64; ++cb)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_shared_v4(sP + uint32_t(cb * L::BLK) + swz(r, c),
-                       make_uint4(pk[cb * 32 + c * 4], pk[cb * 32 + c * 4 + 1], pk[cb * 32 + c * 4 + 2],
-                                  pk[cb * 32 + c * 4 + 3]));
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(BAR(B_P_FULL));
-    }
-    const bool got_last = ok && wait_bar(BAR(B_PV_DONE), uint32_t((ntiles - 1) & 1), abort_flag, a.status);
-    if (__all_sync(0xffffffffu, got_last)) {
-      tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = a.out + ((size_t)(q0 + token) * a.Hq + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tl + uint32_t(2 * kN + c * 32), v);
-        tmem_wait_ld();
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(f2_to_bf2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv),
-                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv),
-                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv),
-                                 f2_to_bf2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv));
-        }
-      }
-      if (valid && a.lse) a.lse[(size_t)(q0 + token) * a.Hq + h] = (m_run + log2f(l_run)) * 0.6931471805599453f;
-    }
-  } else if (warp < kProdWarp) {
-    // ============================ Q preparation, K rotation, V cleaning
-    const int rt = threadIdx.x - 128;
     {
-      const int token = tok0 + rt / G;
-      const int h = g * G + rt % G;
-      const bool valid = token < Lq;
+      const uint32_t sQ = sQ0 + uint32_t(qt * L::QTILE);
       float x[D];
       if (valid) {
         const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)(q0 + token) * a.Hq + h) * D);
@@ -405,7 +325,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           x[c * 8 + 6] = bf_lo(u.w); x[c * 8 + 7] = bf_hi(u.w);
         }
         if constexpr (kRotate) {
-          const uint32_t m = uint32_t(qs + token);
+          const uint32_t m = uint32_t(m_row);
           const bool tab = a.pos.table != nullptr && int(m) < a.pos.max_pos;
 #pragma unroll
           for (int i = 0; i < D / 2; ++i) {
@@ -433,20 +353,116 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int c = 0; c < 8; ++c) {
           const float* y = x + cb * 64 + c * 8;
           if constexpr (kQkF16)
-            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(rt, c),
+            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(r, c),
                          make_uint4(f2_to_h2(y[0], y[1]), f2_to_h2(y[2], y[3]), f2_to_h2(y[4], y[5]),
                                     f2_to_h2(y[6], y[7])));
           else
-            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(rt, c),
+            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(r, c),
                          make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
                                     f2_to_bf2(y[6], y[7])));
         }
       fence_async_smem();
       mbar_arrive(BAR(B_Q_READY));
     }
+    if (qt < nq) {
+      float slope = 0.f;
+      if constexpr (POS == kAlibi) slope = a.pos.slopes[h] * 1.4426950408889634f;
+      const uint32_t tl = tmem + (uint32_t(32 * (warp & 3)) << 16);
+      const uint32_t tS = tl + uint32_t(qt * kN), tO = tl + uint32_t(2 * kN + qt * 128);
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j) {
+        const int slot = j % kSlots;
+        const bool got_s = wait_bar(BAR(B_S_FULL + qt), uint32_t(j & 1), abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
+        tc_fence_after();
+        const bool fast = (POS != kAlibi) && flags[slot * 2];
+        const int* kp = kpos + slot * kN;
+        // the whole S row in registers: four loads, one wait
+        uint32_t v[kN];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        tmem_wait_ld();
+        if (!fast) {
+#pragma unroll
+          for (int e = 0; e < kN; ++e) {
+            float x = __uint_as_float(v[e]);
+            const int p = kp[e];
+            if constexpr (POS == kAlibi) x += slope * float(p - m_row);
+            v[e] = __float_as_uint((p <= m_row) ? x : -INFINITY);
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kN; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        const bool need = mx > m_run + kTau;
+        const float m_new = need ? mx : m_run;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
+        const float2 mneg = make_float2(-m_use, -m_use);
+        float2 sum2 = make_float2(0.f, 0.f);
+        // P packed to bf16 pairs in place: pair e (keys 2e, 2e+1) lands in v[e] (already consumed)
+#pragma unroll
+        for (int e = 0; e < kN / 2; ++e) {
+          float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          x = __fadd2_rn(x, mneg);
+          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+          sum2 = __fadd2_rn(sum2, ev);
+          v[e] = f2_to_bf2(ev.x, ev.y);
+        }
+        const float sum = sum2.x + sum2.y;
+        const float alpha = (j > 0 && need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+        l_run = (j == 0) ? sum : l_run * alpha + sum;
+        // O rescale: PV of the previous tile is complete (the S commit waited for covers it)
+        if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + uint32_t(c * 32), o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + uint32_t(c * 32), o);
+          }
+        }
+        m_run = m_new;
+        // P row -> TMEM over the first 64 columns of S (column e holds keys 2e, 2e+1)
+        tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(v + 0));
+        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(BAR(B_P_FULL + qt));
+      }
+      const bool got_last = ok && wait_bar(BAR(B_FINAL), 0, abort_flag, a.status);
+      if (__all_sync(0xffffffffu, got_last)) {
+        tc_fence_after();
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16* orow = a.out + ((size_t)(q0 + token) * a.Hq + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + uint32_t(c * 32), o);
+          tmem_wait_ld();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[q4] = make_uint4(f2_to_bf2(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv),
+                                   f2_to_bf2(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv),
+                                   f2_to_bf2(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv),
+                                   f2_to_bf2(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv));
+          }
+        }
+        if (valid && a.lse) a.lse[(size_t)(q0 + token) * a.Hq + h] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+      }
+    }
+  } else if (warp < kProdWarp) {
+    // ============================ K rotation, V cleaning
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRot));
+    const int rt = threadIdx.x - kRotWarp0 * 32;
     const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
     bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
-    int cleaned[kStages] = {0, 0};  // V_READY phases completed per stage
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, slot = j % kSlots;
       const uint32_t par = uint32_t((j / kStages) & 1);
@@ -517,175 +533,211 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         fence_async_smem();
         mbar_arrive(BAR(B_V_READY + s));
-        ++cleaned[s];
-      }
-    }
-  } else if (warp == kProdWarp) {
-    // ============================ block words + TMA
-    // Issue order K0, K1, V0, K2, V1, ...: a K stage is refilled once its QK^T is done, a V
-    // stage once its PV is done, and no K load waits behind an earlier tile's PV.
-    const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
-    int* pgid = reinterpret_cast<int*>(sm + L::PGID_OFF);
-    auto fetch = [&](int j) -> uint64_t {  // lane < 8: block word of page slot `lane` of tile j
-      const int jb = j * kPagesPerTile + lane;
-      return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
-    };
-    uint64_t w_next = fetch(0);
-    int issued_k = 0, issued_v = 0;
-    // K of tile j: wait for its stage, publish the tile's metadata, load the pages
-    auto issue_k = [&](int j) -> bool {
-      const int s = j % kStages, slot = j % kSlots;
-      const uint64_t w = w_next;
-      w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
-      int rows = 0, start = 0, page = 0, delta = 0;
-      const int jb = j * kPagesPerTile + lane;
-      if (lane < kPagesPerTile && jb < nb) {
-        page = int(word_page(w));
-        delta = int(word_delta(w));
-        start = delta + kPage * int(word_pg(w));
-        rows = min(int(word_nvalid(w)), kPage);
-        if (page >= a.num_pages) {
-          set_status(a.status, LAZY_STATUS_BAD_PAGE);
-          rows = 0;
-        }
-      }
-      if (j >= kStages) {
-        const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, freed)) return false;
-      }
-      if (lane < kPagesPerTile) {
-        pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
-        pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int idx = lane * 4 + e, pp = idx >> 4, tt = idx & 15;
-        const int rp = __shfl_sync(0xffffffffu, rows, pp);
-        const int sp = __shfl_sync(0xffffffffu, start, pp);
-        kpos[slot * kN + idx] = tt < rp ? sp + tt : INT_MAX;
-      }
-      const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
-      const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
-      if (lane == 0) {
-        flags[slot * 2] = all16 && (last_start + kPage - 1 <= m_min);  // every key visible to every row
-        flags[slot * 2 + 1] = !all16;                                  // some V rows must be cleared
-      }
-      __syncwarp();
-      uint32_t bytes = 0;
-      for (int pp = 0; pp < kPagesPerTile; ++pp)
-        if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += uint32_t(kPage) * D * 2;
-      const uint32_t sK = sK0 + uint32_t(s * L::TILE);
-      if (lane == 0) mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
-      __syncwarp();
-      if (lane < kPagesPerTile && rows > 0)  // one lane per page: TMA issue is per-instruction bound
-#pragma unroll
-        for (int cb = 0; cb < L::CB; ++cb)
-          tma_load_2d(sK + uint32_t(cb * L::BLK + lane * kPage * 128), &tmk, cb * 64, (page * a.Hkv + g) * kPage,
-                      BAR(B_K_FULL + s));
-      __syncwarp();
-      issued_k = j + 1;
-      return true;
-    };
-    // V of tile j (its metadata was published with its K)
-    auto issue_v = [&](int j) -> bool {
-      const int s = j % kStages, slot = j % kSlots;
-      if (j >= kStages) {
-        const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, freed)) return false;
-      }
-      const uint32_t sV = sV0 + uint32_t(s * L::TILE);
-      const int pg_id = lane < kPagesPerTile ? pgid[slot * kPagesPerTile + lane] : -1;
-      const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, pg_id >= 0))) * kPage * D * 2;
-      if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
-      __syncwarp();
-      if (pg_id >= 0)
-#pragma unroll
-        for (int cb = 0; cb < L::CB; ++cb)
-          tma_load_2d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
-                      BAR(B_V_FULL + s));
-      __syncwarp();
-      issued_v = j + 1;
-      return true;
-    };
-    bool ok = issue_k(0);
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (j + 1 < ntiles) ok = issue_k(j + 1);
-      if (ok) ok = issue_v(j);
-    }
-    // never leave copies in flight: wait (bounded) for the last loads of every stage
-    if (lane == 0) {
-      for (int j = max(0, issued_k - kStages); j < issued_k; ++j) {
-        const uint32_t bar = BAR(B_K_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
-        const uint64_t t0 = global_ns();
-        while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
-        }
-      }
-      for (int j = max(0, issued_v - kStages); j < issued_v; ++j) {
-        const uint32_t bar = BAR(B_V_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
-        const uint64_t t0 = global_ns();
-        while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
-        }
       }
     }
   } else {
-    // ============================ MMA issue (one thread)
-    if (lane == 0) {
-      constexpr uint32_t IQK = idesc_mma(kM, kN, 0, kQkF16 ? 1 : 0);
-      constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
-      const uint32_t tS = tmem, tO = tmem + 2 * kN;
-      bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
-      int cleaned[kStages] = {0, 0};  // V_READY phases consumed per stage
-      bool clean_prev = false;        // clean flag of the tile whose PV is issued next
-      auto issue_pv = [&](int jj, bool clean) -> bool {
-        const int s = jj % kStages;
-        const uint32_t par = uint32_t((jj / kStages) & 1);
-        if (!wait_bar(BAR(B_P_FULL), uint32_t(jj & 1), abort_flag, a.status)) return false;
-        if (!wait_bar(BAR(B_V_FULL + s), par, abort_flag, a.status)) return false;
-        if (clean) {
-          if (!wait_bar(BAR(B_V_READY + s), uint32_t(cleaned[s] & 1), abort_flag, a.status)) return false;
-          ++cleaned[s];
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+    if (warp == kProdWarp) {
+      // ============================ block words + TMA
+      // Issue order K0, K1, V0, K2, V1, ...: a K stage is refilled once both its QK^T are done, a
+      // V stage once both its PV are done, and no K load waits behind an earlier tile's PV.
+      const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
+      int* pgid = reinterpret_cast<int*>(sm + L::PGID_OFF);
+      auto fetch = [&](int j) -> uint64_t {  // lane < 8: block word of page slot `lane` of tile j
+        const int jb = j * kPagesPerTile + lane;
+        return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
+      };
+      uint64_t w_next = fetch(0);
+      int issued_k = 0, issued_v = 0;
+      // K of tile j: wait for its stage, publish the tile's metadata, load the pages
+      auto issue_k = [&](int j) -> bool {
+        const int s = j % kStages, slot = j % kSlots;
+        const uint64_t w = w_next;
+        w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
+        int rows = 0, start = 0, page = 0, delta = 0;
+        const int jb = j * kPagesPerTile + lane;
+        if (lane < kPagesPerTile && jb < nb) {
+          page = int(word_page(w));
+          delta = int(word_delta(w));
+          start = delta + kPage * int(word_pg(w));
+          rows = min(int(word_nvalid(w)), kPage);
+          if (page >= a.num_pages) {
+            set_status(a.status, LAZY_STATUS_BAD_PAGE);
+            rows = 0;
+          }
         }
-        tc_fence_after();
-        const uint32_t sV = sV0 + uint32_t(s * L::TILE);
+        if (j >= kStages) {
+          const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, freed)) return false;
+        }
+        if (lane < kPagesPerTile) {
+          pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
+          pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
+        }
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint64_t ad = sdesc(sP + uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32), 16, 1024);
-          const uint64_t bd = sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024);
-          mma_bf16(tO, ad, bd, IPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int e = 0; e < 4; ++e) {
+          const int idx = lane * 4 + e, pp = idx >> 4, tt = idx & 15;
+          const int rp = __shfl_sync(0xffffffffu, rows, pp);
+          const int sp = __shfl_sync(0xffffffffu, start, pp);
+          kpos[slot * kN + idx] = tt < rp ? sp + tt : INT_MAX;
         }
-        mma_commit(BAR(B_PV_DONE));
-        mma_commit(BAR(B_V_FREE + s));
+        const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
+        const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
+        if (lane == 0) {
+          flags[slot * 2] = all16 && (last_start + kPage - 1 <= m_min);  // every key visible to every row
+          flags[slot * 2 + 1] = !all16;                                  // some V rows must be cleared
+        }
+        __syncwarp();
+        uint32_t bytes = 0;
+        for (int pp = 0; pp < kPagesPerTile; ++pp)
+          if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += uint32_t(kPage) * D * 2;
+        const uint32_t sK = sK0 + uint32_t(s * L::TILE);
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
+        __syncwarp();
+        if (lane < kPagesPerTile && rows > 0)  // one lane per page: TMA issue is per-instruction bound
+#pragma unroll
+          for (int cb = 0; cb < L::CB; ++cb)
+            tma_load_2d(sK + uint32_t(cb * L::BLK + lane * kPage * 128), &tmk, cb * 64, (page * a.Hkv + g) * kPage,
+                        BAR(B_K_FULL + s));
+        __syncwarp();
+        issued_k = j + 1;
         return true;
       };
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int s = j % kStages, sbuf = j & 1;
-        if (!wait_bar(BAR(B_K_READY + s), uint32_t((j / kStages) & 1), abort_flag, a.status)) { ok = false; break; }
-        if (j >= 2 && !wait_bar(BAR(B_S_FREE + sbuf), uint32_t(((j >> 1) - 1) & 1), abort_flag, a.status)) {
-          ok = false;
-          break;
+      // V of tile j (its metadata was published with its K)
+      auto issue_v = [&](int j) -> bool {
+        const int s = j % kStages, slot = j % kSlots;
+        if (j >= kStages) {
+          const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, freed)) return false;
         }
-        tc_fence_after();
-        const bool clean_j = flags[(j % kSlots) * 2 + 1] != 0;  // published before K_FULL of tile j
-        const uint32_t sK = sK0 + uint32_t(s * L::TILE);
+        const uint32_t sV = sV0 + uint32_t(s * L::TILE);
+        const int pg_id = lane < kPagesPerTile ? pgid[slot * kPagesPerTile + lane] : -1;
+        const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, pg_id >= 0))) * kPage * D * 2;
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
+        __syncwarp();
+        if (pg_id >= 0)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
-          mma_bf16(tS + uint32_t(sbuf * kN), sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), IQK,
-                   kk > 0 ? 1u : 0u);
+          for (int cb = 0; cb < L::CB; ++cb)
+            tma_load_2d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
+                        BAR(B_V_FULL + s));
+        __syncwarp();
+        issued_v = j + 1;
+        return true;
+      };
+      bool ok = issue_k(0);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        if (j + 1 < ntiles) ok = issue_k(j + 1);
+        if (ok) ok = issue_v(j);
+      }
+      // never leave copies in flight: wait (bounded) for the last loads of every stage
+      if (lane == 0) {
+        for (int j = max(0, issued_k - kStages); j < issued_k; ++j) {
+          const uint32_t bar = BAR(B_K_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+          const uint64_t t0 = global_ns();
+          while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+          }
         }
-        mma_commit(BAR(B_S_FULL + sbuf));
-        mma_commit(BAR(B_K_FREE + s));
-        if (j >= 1 && !issue_pv(j - 1, clean_prev)) { ok = false; break; }
-        clean_prev = clean_j;
+        for (int j = max(0, issued_v - kStages); j < issued_v; ++j) {
+          const uint32_t bar = BAR(B_V_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+          const uint64_t t0 = global_ns();
+          while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+          }
+        }
       }
-      if (ok) issue_pv(ntiles - 1, clean_prev);
-      // every MMA must be complete before TMEM is released
-      mma_commit(BAR(B_FINAL));
-      const uint64_t t0 = global_ns();
-      while (!mbar_test(BAR(B_FINAL), 0) && global_ns() - t0 < kWaitNs) {
+    } else if (warp == kMmaWarp) {
+      // ============================ MMA issue (one thread)
+      if (lane == 0) {
+        constexpr uint32_t IQK = idesc_mma(kM, kN, 0, kQkF16 ? 1 : 0);
+        constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
+        bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
+        int cleaned[kStages] = {0, 0};  // V_READY phases consumed per stage
+        auto qk = [&](int qt, int j) {  // S_qt = Q_qt K_j^T
+          const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE), sQ = sQ0 + uint32_t(qt * L::QTILE);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
+            mma_bf16(tmem + uint32_t(qt * kN), sdesc(sQ + off, 16, 1024), sdesc(sK + off, 16, 1024), IQK,
+                     kk > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR(B_S_FULL + qt));
+        };
+        auto pv = [&](int qt, int jj) {  // O_qt += P_qt V_jj, P from TMEM (8 columns per 16 keys)
+          const uint32_t sV = sV0 + uint32_t((jj % kStages) * L::TILE);
+#pragma unroll
+          for (int kk = 0; kk < kN / 16; ++kk)
+            mma_ts(tmem + uint32_t(2 * kN + qt * 128), tmem + uint32_t(qt * kN + kk * 8),
+                   sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (jj > 0 || kk > 0) ? 1u : 0u);
+        };
+        auto wait_v = [&](int jj, bool clean) -> bool {
+          const int s = jj % kStages;
+          if (!wait_bar(BAR(B_V_FULL + s), uint32_t((jj / kStages) & 1), abort_flag, a.status)) return false;
+          if (clean) {
+            if (!wait_bar(BAR(B_V_READY + s), uint32_t(cleaned[s] & 1), abort_flag, a.status)) return false;
+            ++cleaned[s];
+          }
+          return true;
+        };
+        bool clean_prev = false;  // clean flag of the tile whose PV is issued next
+        if (ok) ok = wait_bar(BAR(B_K_READY), 0, abort_flag, a.status);
+        if (ok) {
+          tc_fence_after();
+          clean_prev = flags[1] != 0;  // published before K_FULL of tile 0
+          qk(0, 0);
+          if (nq == 2) qk(1, 0);
+          mma_commit(BAR(B_K_FREE));
+        }
+        for (int j = 1; j < ntiles && ok; ++j) {
+          const int s = j % kStages, sp = (j - 1) % kStages;
+          if (!wait_bar(BAR(B_P_FULL), uint32_t((j - 1) & 1), abort_flag, a.status) || !wait_v(j - 1, clean_prev)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          pv(0, j - 1);
+          if (!wait_bar(BAR(B_K_READY + s), uint32_t((j / kStages) & 1), abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool clean_j = flags[(j % kSlots) * 2 + 1] != 0;
+          qk(0, j);
+          if (nq == 2) {
+            if (!wait_bar(BAR(B_P_FULL + 1), uint32_t((j - 1) & 1), abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv(1, j - 1);
+          }
+          mma_commit(BAR(B_V_FREE + sp));
+          if (nq == 2) qk(1, j);
+          mma_commit(BAR(B_K_FREE + s));
+          clean_prev = clean_j;
+        }
+        if (ok) {
+          const int jl = ntiles - 1;
+          ok = wait_bar(BAR(B_P_FULL), uint32_t(jl & 1), abort_flag, a.status) && wait_v(jl, clean_prev);
+          if (ok) {
+            tc_fence_after();
+            pv(0, jl);
+          }
+          if (ok && nq == 2) {
+            ok = wait_bar(BAR(B_P_FULL + 1), uint32_t(jl & 1), abort_flag, a.status);
+            if (ok) {
+              tc_fence_after();
+              pv(1, jl);
+            }
+          }
+          if (ok) mma_commit(BAR(B_V_FREE + jl % kStages));
+        }
+        // every MMA must be complete before TMEM is released (and before the epilogue reads O)
+        mma_commit(BAR(B_FINAL));
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(BAR(B_FINAL), 0) && global_ns() - t0 < kWaitNs) {
+        }
       }
+      __syncwarp();
     }
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -745,9 +797,21 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
     LAZY_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM));
     attr[dev & 63] = true;
   }
+  // The warpgroups re-split the launch allocation with setmaxnreg; that split is only valid
+  // (and a growing warpgroup only ever gets its registers) if the kernel launches with exactly
+  // kRegsLaunch registers per thread.
+  static int regs[64] = {};
+  if (!regs[dev & 63]) {
+    cudaFuncAttributes fa;
+    LAZY_CUDA_TRY(cudaFuncGetAttributes(&fa, kern));
+    regs[dev & 63] = fa.numRegs;
+  }
+  if (regs[dev & 63] != tc::kRegsLaunch)
+    return fail(LAZY_ECUDA, "prefill kernel built with %d registers per thread, expected %d", regs[dev & 63],
+                tc::kRegsLaunch);
   const int G = a.Hq / a.Hkv;
-  const int tpt = tc::kM / G;
-  dim3 grid((max_q + tpt - 1) / tpt, a.Hkv, a.B);
+  const int rows_tok = tc::kQT * (tc::kM / G);  // tokens per CTA
+  dim3 grid((max_q + rows_tok - 1) / rows_tok, a.Hkv, a.B);
   kern<<<grid, tc::kThreads, L::SMEM, st>>>(mk, mv, a);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
