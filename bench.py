@@ -67,6 +67,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
     p.add_argument("--pos", default=None, help="override positional kind (e.g. none for the Delta=0 twin)")
+    p.add_argument("--no-overhead", action="store_true", help="skip the deferred-rotation overhead runs")
     return p.parse_args()
 
 
@@ -363,9 +364,63 @@ def run_ours(args, dist):
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if not args.no_overhead and pb.cfg.kind in (lk.POS_ROPE, lk.POS_YARN):
+        res["rotation_overhead"] = rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush)
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, pb, pre, decs, out_p, outs_d, graph, run_step, stream, dist, tokens_per_step)
     return res
+
+
+def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
+    """Deferred-rotation cost: the same attention launches over the same caches with
+    (rot) the workload's rotary kind, (delta0) the kernels built without any positional work
+    (the Delta = 0 twin), and (same_delta) the rotary kernels with every block's Delta set to 0,
+    so that no document boundary occurs.  Eager launches, L2 flushed before each, median of
+    the repetitions; overhead = t_rot / t_delta0 - 1."""
+    import numpy as np
+    import torch
+    cfg_none = lk.pos_cfg_from("none", pb.D)
+    meta0_h = pb.meta_h & ~np.uint64(0xFFFFFF << 16)  # Delta field cleared
+    meta0 = torch.from_numpy(meta0_h.view(np.int64)).to(pb.meta.device)
+    variants = {"rot": (pb.cfg, pb.meta), "delta0": (cfg_none, pb.meta), "same_delta": (pb.cfg, meta0)}
+    reps = max(5, min(args.steps, 20))
+    dec_idx = list(range(0, len(decs), max(1, len(decs) // 8)))[:8]
+    out = {}
+    for phase in ("prefill", "decode"):
+        if (phase == "prefill" and pre is None) or (phase == "decode" and not decs):
+            continue
+        med = {}
+        for name, (cfg, meta) in variants.items():
+            ts = []
+            for r in range(reps + 2):
+                for t in ([None] if phase == "prefill" else dec_idx):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    with torch.cuda.stream(stream):
+                        flush.zero_()
+                        e0.record(stream)
+                        if phase == "prefill":
+                            lk.attn_prefill(pre["q"], pb.cu_q, pb.q_start, pb.doc_blocks, meta, pb.k_cache,
+                                            pb.v_cache, cfg, out_p[: pb.total_q], pb.max_q, ws=pb.ws, stream=stream)
+                        else:
+                            d = decs[t]
+                            lk.attn_decode(d["q"], d["seq_len"], pb.q_start, pb.doc_blocks, meta, pb.k_cache,
+                                           pb.v_cache, cfg, outs_d[t], ws=pb.ws, stream=stream)
+                        e1.record(stream)
+                    stream.synchronize()
+                    if r >= 2:
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+            med[name] = statistics.median(ts)
+        out[phase] = {"rot_us": med["rot"], "delta0_us": med["delta0"], "same_delta_us": med["same_delta"],
+                      "overhead": med["rot"] / med["delta0"] - 1.0,
+                      "boundary_share": (med["rot"] - med["same_delta"]) / med["delta0"]}
+    status = lk.device_status()
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the overhead runs")
+    out["method"] = ("same caches and inputs; rot = rotary kind of the workload, delta0 = kernels "
+                     "without positional work, same_delta = rotary kernels with every Delta = 0; "
+                     f"eager launches, L2 flushed before each, median of {reps} reps"
+                     + (f", decode steps {dec_idx}" if decs else ""))
+    return out
 
 
 def launches_of(phase: str, pb) -> int:
