@@ -446,7 +446,7 @@ int decode_group(int Hq, int Hkv) {
 int choose_splits(int rows, int Hq, int Hkv, int max_blocks) {
   const int G = decode_group(Hq, Hkv);
   const long long units = (long long)rows * (Hq / G);
-  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // CTAs resident at once
+  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // tuned wave unit (not occupancy)
   // About 4 waves of resident CTAs, but at least 16 pages per warp: measured on GB300, long
   // per-warp page runs beat more, shorter CTAs (every CTA pays a pipeline start-up and its
   // split partials), and a partial last wave costs little once there are several waves.
@@ -458,8 +458,29 @@ int choose_splits(int rows, int Hq, int Hkv, int max_blocks) {
   return int(s);
 }
 
+// Wide head groups (MQA-like, G >= 16): per page the CUDA-core kernel would spread the group
+// over G/8 CTAs that each re-read K/V and spend G x 4 KB of FMAs per page, so these rows go
+// to the tensor-core kernel instead, with the G heads of the new token as its query rows.
+bool use_tc_decode(int Hq, int Hkv, int D) {
+  const int G = Hq / Hkv;
+  return G >= 16 && 128 % G == 0 && (D == 64 || D == 128);
+}
+
+// Key-range splits of the tensor-core decode: one wave of single-CTA-per-SM units, at least
+// four 128-key tiles per split.
+int tc_decode_splits(int B, int Hkv, int max_blocks) {
+  const long long units = (long long)B * Hkv;
+  const int tiles = (max_blocks + 7) / 8;
+  long long s = sm_count() / (units > 0 ? units : 1);
+  if (s > tiles / 4) s = tiles / 4;
+  if (s < 1) s = 1;
+  if (s > 64) s = 64;
+  return int(s);
+}
+
 size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks) {
-  const int S = choose_splits(rows, Hq, Hkv, max_blocks);
+  const int S = use_tc_decode(Hq, Hkv, D) ? tc_decode_splits(rows, Hkv, max_blocks)
+                                          : choose_splits(rows, Hq, Hkv, max_blocks);
   if (S <= 1) return 0;
   const size_t po = (size_t)rows * Hq * S * D * 4;
   const size_t pml = (size_t)rows * Hq * S * 2 * 4;
@@ -509,6 +530,28 @@ static int launch_g(const DecodeArgs& a, cudaStream_t st) {
 }
 
 int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (!rows_mode && use_tc_decode(a.Hq, a.Hkv, D)) {
+    a.S = tc_decode_splits(a.rows, a.Hkv, a.max_blocks);
+    if (a.S > 1) {
+      const size_t need = decode_ws_bytes(a.rows, a.Hq, a.Hkv, D, a.max_blocks);
+      if (!ws || ws_bytes < need)
+        return fail(LAZY_EINVAL, "workspace too small: need %zu bytes, got %zu", need, ws_bytes);
+      if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(LAZY_EINVAL, "workspace must be 256-byte aligned");
+      const size_t po = (size_t)a.rows * a.Hq * a.S * D * 4;
+      a.part_o = static_cast<float*>(ws);
+      a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((po + 255) / 256) * 256);
+    }
+    int rc = run_prefill_tc(a.q, nullptr, a.q_start, a.doc_blocks, a.meta, a.B, a.max_blocks, 1, a.k_cache,
+                            a.v_cache, a.num_pages, a.Hq, a.Hkv, D, a.pos, a.out, a.lse, st, a.seq_len, a.S,
+                            a.part_o, a.part_ml);
+    if (rc || a.S == 1) return rc;
+    if (D == 128)
+      merge_kernel<128><<<(unsigned)a.rows * a.Hq, 128, 0, st>>>(a.part_o, a.part_ml, a.S, a.Hq, a.out, a.lse);
+    else
+      merge_kernel<64><<<(unsigned)a.rows * a.Hq, 64, 0, st>>>(a.part_o, a.part_ml, a.S, a.Hq, a.out, a.lse);
+    LAZY_CUDA_TRY(cudaGetLastError());
+    return LAZY_OK;
+  }
   a.group = decode_group(a.Hq, a.Hkv);
   const int G = a.Hq / a.Hkv;
   if (G % a.group != 0) return fail(LAZY_EINVAL, "Hq/Hkv = %d not supported", G);

@@ -30,6 +30,10 @@ size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks);
 int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
                    const uint64_t* meta, int B, int max_blocks, int max_q, const void* k_cache,
                    const void* v_cache, int num_pages, int Hq, int Hkv, int D, const PosParams& pos, void* out,
-                   float* lse, cudaStream_t st);
+                   float* lse, cudaStream_t st, const int32_t* seq_len = nullptr, int S = 1,
+                   float* part_o = nullptr, float* part_ml = nullptr);
+// decode of wide head groups (Hq/Hkv >= 16) runs on the tensor-core kernel in decode mode
+bool use_tc_decode(int Hq, int Hkv, int D);
+int tc_decode_splits(int B, int Hkv, int max_blocks);
 
 }  // namespace lazykv

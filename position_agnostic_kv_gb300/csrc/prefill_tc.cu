@@ -28,6 +28,8 @@
 //              commit that signals S_i(j+1) also covers PV_i(j).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64 of S_i.
 // GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
+// Decode mode serves wide head groups (MQA): the G heads of one new token fill the rows, the
+// key range is split over several CTAs and their partials are merged by log-sum-exp.
 // Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
 #include <cfloat>
 #include <climits>
@@ -108,6 +110,12 @@ struct Args {
   float* lse;
   uint32_t* status;
   PosParams pos;
+  // decode mode (seq_len != null): one query row per request at m = seq_len - 1, the key range
+  // split over S CTAs whose unnormalised partials (O, base-2 max, sum) go to part_o / part_ml
+  const int32_t* seq_len;
+  int S;
+  float* part_o;   // [B][Hq][S][D]
+  float* part_ml;  // [B][Hq][S][2]
 };
 
 // ---------------------------------------------------------------- tcgen05 / TMA wrappers
@@ -243,23 +251,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* sm = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mp = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int split = int(blockIdx.x) % a.S, mp = int(blockIdx.x) / a.S, g = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv;
   const int tpt = kM / G;  // tokens per Q tile
-  const int q0 = a.cu_q[b];
-  const int Lq = a.cu_q[b + 1] - q0;
+  const int qs = a.q_start[b];
+  const bool dec = a.seq_len != nullptr;
+  const int q0 = dec ? b : a.cu_q[b];                      // first query row of the request
+  const int Lq = dec ? 1 : a.cu_q[b + 1] - q0;
+  const int mbase = dec ? a.seq_len[b] - 1 : qs;           // absolute position of its token 0
   const int tok0 = mp * kQT * tpt;
   if (tok0 >= Lq) return;  // uniform for the CTA, before any barrier or TMEM use
   const int nq = (tok0 + tpt < Lq) ? 2 : 1;  // live Q tiles
-  const int qs = a.q_start[b];
   const int ntok = min(kQT * tpt, Lq - tok0);
-  const int m_min = qs + tok0, m_max = qs + tok0 + ntok - 1;
+  const int m_min = mbase + tok0, m_max = mbase + tok0 + ntok - 1;
   int nb = a.doc_blocks[b] + (m_max - qs) / kPage + 1;
   if (nb > a.max_blocks) {
     if (threadIdx.x == 0) set_status(a.status, LAZY_STATUS_BAD_ROW);
     nb = a.max_blocks;
   }
-  const int ntiles = (nb + kPagesPerTile - 1) / kPagesPerTile;
+  const int ntiles_all = (nb + kPagesPerTile - 1) / kPagesPerTile;
+  const int chunk = (ntiles_all + a.S - 1) / a.S;
+  const int t0 = split * chunk;                            // first K/V tile of this CTA
+  const int ntiles = min(ntiles_all, t0 + chunk) - t0;
+  if (ntiles <= 0) {  // an empty split contributes a neutral partial (uniform for the CTA)
+    for (int i = threadIdx.x; i < ntok * G; i += blockDim.x) {
+      const size_t pi = ((size_t)(q0 + tok0 + i / G) * a.Hq + g * G + i % G) * a.S + split;
+      a.part_ml[pi * 2] = -INFINITY;
+      a.part_ml[pi * 2 + 1] = 0.f;
+      for (int c = 0; c < D; ++c) a.part_o[pi * D + c] = 0.f;
+    }
+    return;
+  }
 
   const uint32_t sQ0 = sb + L::Q_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
   int* kpos = reinterpret_cast<int*>(sm + L::KPOS_OFF);
@@ -310,7 +332,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int token = tok0 + qt * tpt + r / G;
     const int h = g * G + r % G;
     const bool valid = token < Lq;
-    const int m_row = valid ? qs + token : -1;
+    const int m_row = valid ? mbase + token : -1;
     {
       const uint32_t sQ = sQ0 + uint32_t(qt * L::QTILE);
       float x[D];
@@ -435,7 +457,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         mbar_arrive(BAR(B_P_FULL + qt));
       }
       const bool got_last = ok && wait_bar(BAR(B_FINAL), 0, abort_flag, a.status);
-      if (__all_sync(0xffffffffu, got_last)) {
+      if (__all_sync(0xffffffffu, got_last) && a.S > 1) {
+        tc_fence_after();
+        const size_t pi = ((size_t)(q0 + token) * a.Hq + h) * a.S + split;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + uint32_t(c * 32), o);
+          tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + pi * D + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[q4 * 4]), __uint_as_float(o[q4 * 4 + 1]),
+                                    __uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3]));
+          }
+        }
+        if (valid) {
+          a.part_ml[pi * 2] = l_run > 0.f ? m_run : -INFINITY;
+          a.part_ml[pi * 2 + 1] = l_run;
+        }
+      } else if (__all_sync(0xffffffffu, got_last)) {
         tc_fence_after();
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         __nv_bfloat16* orow = a.out + ((size_t)(q0 + token) * a.Hq + h) * D;
@@ -544,7 +586,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
       int* pgid = reinterpret_cast<int*>(sm + L::PGID_OFF);
       auto fetch = [&](int j) -> uint64_t {  // lane < 8: block word of page slot `lane` of tile j
-        const int jb = j * kPagesPerTile + lane;
+        const int jb = (t0 + j) * kPagesPerTile + lane;
         return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
       };
       uint64_t w_next = fetch(0);
@@ -555,7 +597,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const uint64_t w = w_next;
         w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
         int rows = 0, start = 0, page = 0, delta = 0;
-        const int jb = j * kPagesPerTile + lane;
+        const int jb = (t0 + j) * kPagesPerTile + lane;
         if (lane < kPagesPerTile && jb < nb) {
           page = int(word_page(w));
           delta = int(word_delta(w));
@@ -788,6 +830,7 @@ static int cache_map(CUtensorMap* map, const void* base, int num_pages, int Hkv,
 
 template <int D, int POS>
 static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q, cudaStream_t st) {
+  // (decode mode: max_q = 1, one query row per request)
   using L = tc::Layout<D>;
   auto kern = tc::prefill_tc_kernel<D, POS>;
   static bool attr[64] = {};
@@ -811,7 +854,7 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
                 tc::kRegsLaunch);
   const int G = a.Hq / a.Hkv;
   const int rows_tok = tc::kQT * (tc::kM / G);  // tokens per CTA
-  dim3 grid((max_q + rows_tok - 1) / rows_tok, a.Hkv, a.B);
+  dim3 grid(unsigned((max_q + rows_tok - 1) / rows_tok) * unsigned(a.S), a.Hkv, a.B);
   kern<<<grid, tc::kThreads, L::SMEM, st>>>(mk, mv, a);
   LAZY_CUDA_TRY(cudaGetLastError());
   return LAZY_OK;
@@ -820,8 +863,9 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
 int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
                    const uint64_t* meta, int B, int max_blocks, int max_q, const void* k_cache,
                    const void* v_cache, int num_pages, int Hq, int Hkv, int D, const PosParams& pos, void* out,
-                   float* lse, cudaStream_t st) {
+                   float* lse, cudaStream_t st, const int32_t* seq_len, int S, float* part_o, float* part_ml) {
   const int G = Hq / Hkv;
+  if (S < 1 || (S > 1 && (!seq_len || !part_o || !part_ml))) return fail(LAZY_EINVAL, "bad key-range split");
   if (G > tc::kM || (tc::kM % G) != 0) return fail(LAZY_EINVAL, "Hq/Hkv = %d must divide 128", G);
   CUtensorMap mk, mv;
   int rc = cache_map(&mk, k_cache, num_pages, Hkv, D);
@@ -843,6 +887,11 @@ int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, c
   a.lse = lse;
   a.status = status_word();
   a.pos = pos;
+  a.seq_len = seq_len;
+  a.S = S;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  if (seq_len) max_q = 1;
   const int kind = (pos.kind == kYarn) ? kRope : pos.kind;
   if (D == 128) {
     if (kind == kRope) return launch_tc<128, kRope>(mk, mv, a, max_q, st);

@@ -12,7 +12,7 @@ import oracle
 from oracle import lazy_oracle as lo
 from tests.gpu_common import (assert_close, lib, oracle_caches_for, request_instances)
 from tests.oracle_setup import oracle_meta, raw_segments
-from workloads import PosCfg, make_custom, make_workload
+from workloads import PosCfg, alibi_slopes_input, make_custom, make_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -194,6 +194,22 @@ def test_edge_shapes(lk, D, Hq, Hkv):
     w = make_custom([1, 15, 16, 17, 33], [[4, 0, 2], [1, 3], [2, 4, 1, 0]], Hq, Hkv, D,
                     PosCfg("rope", 1e4, D), [3, 0, 17], 5, seed=D + Hq)
     _run_and_check(lk, w, [0, 1, 2], 5, {0, 4})
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,kind", [(128, 32, 1, "rope"), (64, 16, 1, "alibi"), (128, 32, 2, "yarn")])
+def test_wide_group_decode(lk, D, Hq, Hkv, kind):
+    """Head groups of 16 and 32 (MQA-like) decode on the tensor-core kernel with the key range
+    split over CTAs: one long request (several splits), a 1-token one (empty splits), ragged
+    documents, rotary and ALiBi variants."""
+    if kind == "yarn":
+        pos = PosCfg(kind, 5e5, D, yarn_factor=8.0, yarn_orig_ctx=8192)
+    elif kind == "alibi":
+        pos = PosCfg(kind, 1e4, D, alibi_slopes=alibi_slopes_input(Hq))
+    else:
+        pos = PosCfg(kind, 1e4, D)
+    w = make_custom([2900, 700, 17, 1], [[0, 1, 2], [3], [2, 3, 1]], Hq, Hkv, D, pos, [5, 1, 0], 3,
+                    seed=D + Hq + Hkv)
+    _run_and_check(lk, w, [0, 1, 2], 3, {0, 2})
 
 
 def test_sharpened_queries_separate_negative_controls(lk):
