@@ -27,6 +27,8 @@
 //              order, so S_i of tile j+1 is only written after PV_i(j) has read P_i, and the
 //              commit that signals S_i(j+1) also covers PV_i(j).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64 of S_i.
+// With one live Q tile (short queries, decode), S0 and S1 double-buffer that tile's scores
+// instead (tile j in S_{j%2}), so QK^T of tile j+1 runs while the softmax works on tile j.
 // GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
 // Decode mode serves wide head groups (MQA): the G heads of one new token fill the rows, the
 // key range is split over several CTAs and their partials are merged by log-sum-exp.
@@ -71,11 +73,12 @@ enum : int {
   B_V_READY = 8,   // [2] key-less V rows cleared (128 arrivals); only tiles that need it
                    //     complete a phase, so both sides count such tiles per stage
   B_V_FREE = 10,   // [2] both PV done with the V stage (commit)
-  B_S_FULL = 12,   // [2] per Q tile: S written (commit; also covers that tile's previous PV)
-  B_P_FULL = 14,   // [2] per Q tile: P written to TMEM, O rescaled (128 arrivals)
+  B_S_FULL = 12,   // [2] per Q tile (one live tile: per S buffer): S written (commit)
+  B_P_FULL = 14,   // [2] per Q tile (one live tile: per S buffer): P in TMEM, O rescaled (128)
   B_Q_READY = 16,  // both Q tiles prepared (256 arrivals)
   B_FINAL = 17,    // all MMAs finished (commit)
-  NBAR = 18
+  B_PV_DONE = 18,  // one live Q tile only: PV of a tile finished (commit)
+  NBAR = 19
 };
 
 template <int D>
@@ -309,6 +312,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     mbar_init(BAR(B_Q_READY), 2 * 128);
     mbar_init(BAR(B_FINAL), 1);
+    mbar_init(BAR(B_PV_DONE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -390,12 +394,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       float slope = 0.f;
       if constexpr (POS == kAlibi) slope = a.pos.slopes[h] * 1.4426950408889634f;
       const uint32_t tl = tmem + (uint32_t(32 * (warp & 3)) << 16);
-      const uint32_t tS = tl + uint32_t(qt * kN), tO = tl + uint32_t(2 * kN + qt * 128);
+      const uint32_t tO = tl + uint32_t(2 * kN + qt * 128);
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
       for (int j = 0; j < ntiles; ++j) {
         const int slot = j % kSlots;
-        const bool got_s = wait_bar(BAR(B_S_FULL + qt), uint32_t(j & 1), abort_flag, a.status);
+        const int buf = nq == 2 ? qt : (j & 1);  // S/P buffer and its barrier pair
+        const uint32_t tS = tl + uint32_t(buf * kN);
+        const bool got_s =
+            wait_bar(BAR(B_S_FULL + buf), uint32_t(nq == 2 ? (j & 1) : ((j >> 1) & 1)), abort_flag, a.status);
         if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
         tc_fence_after();
         const bool fast = (POS != kAlibi) && flags[slot * 2];
@@ -436,7 +443,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const float sum = sum2.x + sum2.y;
         const float alpha = (j > 0 && need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
         l_run = (j == 0) ? sum : l_run * alpha + sum;
-        // O rescale: PV of the previous tile is complete (the S commit waited for covers it)
+        // O rescale needs the previous tile's PV complete: with two Q tiles the S commit waited
+        // for covers it; with one, S of tile j was issued before PV of tile j-1, so wait for it
+        if (nq == 1 && j > 0) {
+          const bool got_pv = wait_bar(BAR(B_PV_DONE), uint32_t((j - 1) & 1), abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, got_pv)) { ok = false; break; }
+          tc_fence_after();
+        }
         if (__any_sync(0xffffffffu, j > 0 && alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -454,7 +467,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(BAR(B_P_FULL + qt));
+        mbar_arrive(BAR(B_P_FULL + buf));
       }
       const bool got_last = ok && wait_bar(BAR(B_FINAL), 0, abort_flag, a.status);
       if (__all_sync(0xffffffffu, got_last) && a.S > 1) {
@@ -720,6 +733,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           return true;
         };
         bool clean_prev = false;  // clean flag of the tile whose PV is issued next
+        if (nq == 1) {
+          // one live Q tile: tile j's scores in S_{j%2}; order QK(0) QK(1) | PV(0) QK(2) | PV(1) ...
+          bool clean[2] = {false, false};  // clean flags of the tiles whose QK is issued, by j % 2
+          auto qk1 = [&](int j) -> bool {
+            if (!wait_bar(BAR(B_K_READY + j % kStages), uint32_t((j / kStages) & 1), abort_flag, a.status))
+              return false;
+            tc_fence_after();
+            clean[j & 1] = flags[(j % kSlots) * 2 + 1] != 0;
+            const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
+              mma_bf16(tmem + uint32_t((j & 1) * kN), sdesc(sQ0 + off, 16, 1024), sdesc(sK + off, 16, 1024), IQK,
+                       kk > 0 ? 1u : 0u);
+            }
+            mma_commit(BAR(B_S_FULL + (j & 1)));
+            mma_commit(BAR(B_K_FREE + j % kStages));
+            return true;
+          };
+          if (ok) ok = qk1(0);
+          if (ok && ntiles > 1) ok = qk1(1);
+          for (int j = 0; j < ntiles && ok; ++j) {
+            ok = wait_bar(BAR(B_P_FULL + (j & 1)), uint32_t((j >> 1) & 1), abort_flag, a.status) &&
+                 wait_v(j, clean[j & 1]);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t sV = sV0 + uint32_t((j % kStages) * L::TILE);
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk)
+              mma_ts(tmem + uint32_t(2 * kN), tmem + uint32_t((j & 1) * kN + kk * 8),
+                     sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(BAR(B_PV_DONE));
+            mma_commit(BAR(B_V_FREE + j % kStages));
+            if (j + 2 < ntiles) ok = qk1(j + 2);
+          }
+          ok = false;  // the two-tile schedule below is skipped
+        }
         if (ok) ok = wait_bar(BAR(B_K_READY), 0, abort_flag, a.status);
         if (ok) {
           tc_fence_after();
