@@ -54,14 +54,15 @@ constexpr int kThreads = 512;
 constexpr int kRotWarp0 = 8;
 constexpr int kProdWarp = 12;
 constexpr int kMmaWarp = 13;
-// registers per thread after the re-split (no spills at this split):
-// 2*128*184 + 128*56 + 128*88 = 65536 = 512 * 128
+// Registers per thread after the re-split, per warpgroup role (the splits with no spills):
+// kernels that rotate K give the rotation warps more (2*128*184 + 128*56 + 128*88), the others
+// give the softmax more (2*128*192 + 128*48 + 128*80); both add up to 512 * 128 = 65536.
 constexpr int kRegsLaunch = 128;
-constexpr int kRegsSoftmax = 184;
-constexpr int kRegsRot = 56;
-constexpr int kRegsIssue = 88;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsRot + 128 * kRegsIssue == kThreads * kRegsLaunch,
-              "warpgroup register shares must add up to the launch allocation");
+template <bool ROT> struct Regs {
+  static constexpr int softmax = ROT ? 184 : 192, rot = ROT ? 56 : 48, issue = ROT ? 88 : 80;
+  static_assert(2 * 128 * softmax + 128 * rot + 128 * issue == kThreads * kRegsLaunch,
+                "warpgroup register shares must add up to the launch allocation");
+};
 constexpr float kTau = 8.0f;
 
 // barrier indices
@@ -90,8 +91,8 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + kQT * QTILE;        // K ring
   static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
-  static constexpr int KPOS_OFF = V_OFF + kStages * TILE;  // int [slot][128] key positions
-  static constexpr int PINFO_OFF = KPOS_OFF + kSlots * kN * 4;          // int2 [slot][8] {Delta, rows}
+  static constexpr int PSTART_OFF = V_OFF + kStages * TILE;  // int [slot][8] first key position per page
+  static constexpr int PINFO_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, rows}
   static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, clean}
   static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] physical pages
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
@@ -287,7 +288,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   }
 
   const uint32_t sQ0 = sb + L::Q_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
-  int* kpos = reinterpret_cast<int*>(sm + L::KPOS_OFF);
+  int* pstart = reinterpret_cast<int*>(sm + L::PSTART_OFF);
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
   unsigned long long* turns = reinterpret_cast<unsigned long long*>(sm + L::TURNS_OFF);
@@ -330,7 +331,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
   if (warp < 2 * 4) {
     // ============================ Q preparation, softmax and epilogue of Q tile qt
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::softmax));
     const int qt = warp >> 2;
     const int r = threadIdx.x & (kM - 1);  // row of the tile = TMEM lane
     const int token = tok0 + qt * tpt + r / G;
@@ -406,7 +407,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
         tc_fence_after();
         const bool fast = (POS != kAlibi) && flags[slot * 2];
-        const int* kp = kpos + slot * kN;
         // the whole S row in registers: four loads, one wait
         uint32_t v[kN];
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
@@ -414,13 +414,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
         tmem_wait_ld();
-        if (!fast) {
+        if (!fast) {  // key p = start + t of a page is visible iff t < rows and p <= m
 #pragma unroll
-          for (int e = 0; e < kN; ++e) {
-            float x = __uint_as_float(v[e]);
-            const int p = kp[e];
-            if constexpr (POS == kAlibi) x += slope * float(p - m_row);
-            v[e] = __float_as_uint((p <= m_row) ? x : -INFINITY);
+          for (int pp = 0; pp < kPagesPerTile; ++pp) {
+            const int st = pstart[slot * kPagesPerTile + pp];
+            const int lim = min(pinfo[slot * kPagesPerTile + pp].y, m_row - st + 1);
+            float base = 0.f;
+            if constexpr (POS == kAlibi) base = slope * float(st - m_row);
+#pragma unroll
+            for (int t = 0; t < kPage; ++t) {
+              float x = __uint_as_float(v[pp * kPage + t]);
+              if constexpr (POS == kAlibi) x += fmaf(slope, float(t), base);
+              v[pp * kPage + t] = __float_as_uint(t < lim ? x : -INFINITY);
+            }
           }
         }
         float mx = -INFINITY;
@@ -514,7 +520,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   } else if (warp < kProdWarp) {
     // ============================ K rotation, V cleaning
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRot));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::rot));
     const int rt = threadIdx.x - kRotWarp0 * 32;
     const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
     bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
@@ -591,7 +597,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::issue));
     if (warp == kProdWarp) {
       // ============================ block words + TMA
       // Issue order K0, K1, V0, K2, V1, ...: a K stage is refilled once both its QK^T are done, a
@@ -628,13 +634,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (lane < kPagesPerTile) {
           pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
           pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int idx = lane * 4 + e, pp = idx >> 4, tt = idx & 15;
-          const int rp = __shfl_sync(0xffffffffu, rows, pp);
-          const int sp = __shfl_sync(0xffffffffu, start, pp);
-          kpos[slot * kN + idx] = tt < rp ? sp + tt : INT_MAX;
+          pstart[slot * kPagesPerTile + lane] = start;
         }
         const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
         const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
