@@ -126,3 +126,36 @@ class PagedBatch:
         attn_decode(inp["q"], inp["seq_len"], self.q_start, self.doc_blocks, self.meta,
                     self.k_cache, self.v_cache, self.cfg, out, lse=lse, ws=self.ws)
         return out
+
+
+# -------------------------------------------------------------------- cold documents
+def encode_document(q, k, v, pages, k_cache, v_cache, cfg, ws=None, out=None):
+    """Cold-document processing: the first time a document is seen it is encoded alone, from
+    local position 0 ([NOTE] 整体框架: each document's cache is built independently, indexed
+    from 0).  Its keys (rotated by their local positions) and values are written into
+    ``pages`` of the position-free cache, then the document's own causal attention runs as a
+    request with no cached documents whose query segment is the document (Delta = 0).
+
+    q, k, v: bf16 [L, Hq | Hkv, D] raw projections of the document's tokens; pages: int list
+    of ceil(L / 16) physical page ids.  Returns the attention output [L, Hq, D] (bf16); the
+    cached pages can then be reused by any later request at any document offset."""
+    L, Hq, D = q.shape
+    dev = q.device
+    pages = np.asarray(pages, dtype=np.int32)
+    if len(pages) * PAGE < L:
+        raise ValueError("encode_document: fewer pages than the document needs")
+    t = np.arange(L, dtype=np.int32)
+    kv_write(k, v, i32(pages[t // PAGE] * PAGE + t % PAGE, dev), i32(t, dev), k_cache, v_cache, cfg)
+    max_blocks = len(pages)
+    _, meta_h, _, q_start_h, doc_blocks_h = build_doc_meta(
+        [0, 0], [], [], [0], [], [L], [0, len(pages)], pages, max_blocks)
+    meta = torch.from_numpy(meta_h.view(np.int64)).to(dev)
+    if out is None:
+        out = torch.empty((L, Hq, D), dtype=torch.bfloat16, device=dev)
+    Hkv = k_cache.shape[1]
+    if ws is None:
+        n = workspace_size(PHASE_PREFILL, L, 1, max_blocks, Hq, Hkv, D)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    attn_prefill(q, i32([0, L], dev), i32(q_start_h, dev), i32(doc_blocks_h, dev), meta, k_cache,
+                 v_cache, cfg, out, L, ws=ws)
+    return out

@@ -12,7 +12,7 @@ import oracle
 from oracle import lazy_oracle as lo
 from tests.gpu_common import (assert_close, lib, oracle_caches_for, request_instances)
 from tests.oracle_setup import oracle_meta, raw_segments
-from workloads import PosCfg, alibi_slopes_input, make_custom, make_workload
+from workloads import PosCfg, alibi_slopes_input, f32_to_bf16_bits, make_custom, make_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -210,6 +210,86 @@ def test_wide_group_decode(lk, D, Hq, Hkv, kind):
     w = make_custom([2900, 700, 17, 1], [[0, 1, 2], [3], [2, 3, 1]], Hq, Hkv, D, pos, [5, 1, 0], 3,
                     seed=D + Hq + Hkv)
     _run_and_check(lk, w, [0, 1, 2], 3, {0, 2})
+
+
+def test_long_context_128k(lk):
+    """Long context: a 32 768-token document (the page-in-document field's maximum, pg 2047),
+    six of 16 384 tokens and one of 5 000, shuffled into one 136 072-token prompt; the query and
+    decode tokens sit at absolute positions ~1.36e5 (exact-turn angles, 24-bit Delta)."""
+    w = make_custom([32768, 16384, 16384, 16384, 16384, 16384, 16384, 5000],
+                    [[3, 0, 7, 1, 6, 2, 5, 4]], 8, 2, 128, PosCfg("rope", 5e5, 128), [16], 2,
+                    seed=1280)
+    assert int(oracle_meta(w)[2][0]) == 136072 + 16
+    _run_and_check(lk, w, [0], 2, {0, 1})
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,L", [(128, 8, 2, 200), (64, 4, 4, 33), (128, 32, 1, 130)])
+def test_cold_document_encode_then_reuse(lk, D, Hq, Hkv, L):
+    """A document seen for the first time is encoded alone from local position 0 (keys written
+    at local positions, its own causal attention at Delta = 0); the written pages are then the
+    document's cache, which a later request reuses at a non-zero offset."""
+    import torch
+    from position_agnostic_kv_gb300.runner import bits_to_tensor, encode_document
+    rng = np.random.default_rng([L, D, Hq])
+    bf = lambda *shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    pos = PosCfg("rope", 1e4, D)
+    q, k, v = bf(L, Hq, D), bf(L, Hkv, D), bf(L, Hkv, D)
+    n_pages = (L + 15) // 16
+    pages = rng.permutation(3 * n_pages)[:n_pages].astype(np.int32)
+    dev = torch.device("cuda")
+    kc = torch.zeros((3 * n_pages, Hkv, 16, D), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    cfg = lk.pos_cfg_from("rope", D, rope_theta=1e4)
+    out = encode_document(bits_to_tensor(q, dev), bits_to_tensor(k, dev), bits_to_tensor(v, dev),
+                          pages, kc, vc, cfg)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    ref, _ = lo.materialized_attention([(lo.bf16_bits_to_f64(k), lo.bf16_bits_to_f64(v))],
+                                       lo.bf16_bits_to_f64(q), np.arange(L), pos.as_dict())
+    assert_close(out, ref, "cold document self-attention")
+    # the written pages are the document's cache: what the oracle writes for the same tokens
+    okc = np.zeros((3 * n_pages, Hkv, 16, D), np.uint16)
+    ovc = np.zeros_like(okc)
+    t = np.arange(L)
+    oracle.kv_write(k, v, pages[t // 16] * 16 + t % 16, t, pos.as_dict(), okc, ovc)
+    np.testing.assert_array_equal(_bits(vc), ovc)
+    gk, rk = lo.bf16_bits_to_f64(_bits(kc)), lo.bf16_bits_to_f64(okc)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(rk), 2.0 ** -126))) - 7)
+    assert not (np.abs(gk - rk) > ulp + 6e-6).any()
+    # reuse: a request [another document of 37 tokens, this document] + a 5-token query
+    pre_len, ql = 37, 5
+    kp, vp, qq, kq, vq = bf(pre_len, Hkv, D), bf(pre_len, Hkv, D), bf(ql, Hq, D), bf(ql, Hkv, D), bf(ql, Hkv, D)
+    kc2 = torch.zeros((3 * n_pages + 8, Hkv, 16, D), dtype=torch.bfloat16, device=dev)
+    vc2 = torch.zeros_like(kc2)
+    kc2[: 3 * n_pages], vc2[: 3 * n_pages] = kc, vc
+    pre_pages = np.array([3 * n_pages, 3 * n_pages + 1, 3 * n_pages + 2], np.int32)
+    q_pages = np.array([3 * n_pages + 3], np.int32)
+    tp = np.arange(pre_len)
+    lk.kv_write(bits_to_tensor(kp, dev), bits_to_tensor(vp, dev),
+                torch.from_numpy((pre_pages[tp // 16] * 16 + tp % 16).astype(np.int32)).to(dev),
+                torch.from_numpy(tp.astype(np.int32)).to(dev), kc2, vc2, cfg)
+    doc_len = [pre_len, L]
+    doc_page_off = [0, len(pre_pages), len(pre_pages) + n_pages]
+    max_blocks = len(pre_pages) + n_pages + 1
+    bt, meta_h, seq_len, q_start, doc_blocks = lk.build_doc_meta(
+        [0, 2], [0, 1], doc_len, doc_page_off, np.concatenate([pre_pages, pages]), [ql], [0, 1],
+        q_pages, max_blocks)
+    tq = np.arange(ql)
+    lk.kv_write(bits_to_tensor(kq, dev), bits_to_tensor(vq, dev),
+                torch.from_numpy((q_pages[0] * 16 + tq).astype(np.int32)).to(dev),
+                torch.from_numpy(tq.astype(np.int32)).to(dev), kc2, vc2, cfg)
+    out2 = torch.empty((ql, Hq, D), dtype=torch.bfloat16, device=dev)
+    i32 = lambda x: torch.from_numpy(np.asarray(x, np.int32)).to(dev)
+    ws = torch.empty(max(lk.workspace_size(lk.PHASE_PREFILL, ql, 1, max_blocks, Hq, Hkv, D), 256),
+                     dtype=torch.uint8, device=dev)
+    lk.attn_prefill(bits_to_tensor(qq, dev), i32([0, ql]), i32(q_start), i32(doc_blocks),
+                    torch.from_numpy(meta_h.view(np.int64)).to(dev), kc2, vc2, cfg, out2, ql, ws=ws)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    segs = [(lo.bf16_bits_to_f64(kp), lo.bf16_bits_to_f64(vp)), (lo.bf16_bits_to_f64(k), lo.bf16_bits_to_f64(v)),
+            (lo.bf16_bits_to_f64(kq), lo.bf16_bits_to_f64(vq))]
+    ref2, _ = lo.materialized_attention(segs, lo.bf16_bits_to_f64(qq), pre_len + L + tq, pos.as_dict())
+    assert_close(out2, ref2, "reuse of the cold-encoded document at offset 37")
 
 
 def test_sharpened_queries_separate_negative_controls(lk):
