@@ -92,7 +92,9 @@ struct Layout {
   static constexpr int K_OFF = Q_OFF + kQT * QTILE;        // K ring
   static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
   static constexpr int PSTART_OFF = V_OFF + kStages * TILE;  // int [slot][8] first key position per page
-  static constexpr int PINFO_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, rows}
+  static constexpr int RUN_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int [slot][8] first page of
+                                                                         // the page's run of equal Delta
+  static constexpr int PINFO_OFF = RUN_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, rows}
   static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, clean}
   static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] physical pages
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
@@ -289,6 +291,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
   const uint32_t sQ0 = sb + L::Q_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
   int* pstart = reinterpret_cast<int*>(sm + L::PSTART_OFF);
+  int* prun = reinterpret_cast<int*>(sm + L::RUN_OFF);
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
   unsigned long long* turns = reinterpret_cast<unsigned long long*>(sm + L::TURNS_OFF);
@@ -533,16 +536,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const uint32_t sK = sK0 + uint32_t(s * L::TILE);
         // cos/sin rows only for pages that start a new document offset: page pp uses the row of
         // the first page of its run of equal Delta (consecutive pages of a document share it)
-        int run_start = 0;
-        if (ok) {
-#pragma unroll
-          for (int pp = 1; pp <= ps; ++pp)
-            if (pinfo[slot * kPagesPerTile + pp].x != pinfo[slot * kPagesPerTile + pp - 1].x) run_start = pp;
-        }
+        const int run_start = ok ? prun[slot * kPagesPerTile + ps] : 0;
         for (int idx = rt; ok && idx < kPagesPerTile * (D / 4); idx += 128) {
           const int pp = idx / (D / 4), q = idx % (D / 4);
           const int dl = pinfo[slot * kPagesPerTile + pp].x;
-          if (pp == 0 || dl != pinfo[slot * kPagesPerTile + pp - 1].x) {
+          if (prun[slot * kPagesPerTile + pp] == pp) {
             float s0, c0, s1, c1;
             turn_sincos(uint32_t(dl), turns[2 * q], s0, c0);
             turn_sincos(uint32_t(dl), turns[2 * q + 1], s1, c1);
@@ -631,10 +629,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
           if (!__all_sync(0xffffffffu, freed)) return false;
         }
+        const int prev_delta = __shfl_up_sync(0xffffffffu, delta, 1);
+        const uint32_t runs = __ballot_sync(0xffffffffu, lane >= 1 && lane < kPagesPerTile && delta != prev_delta);
         if (lane < kPagesPerTile) {
           pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
           pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
           pstart[slot * kPagesPerTile + lane] = start;
+          const uint32_t upto = runs & ((2u << lane) - 1u);  // run starts at or before this page
+          prun[slot * kPagesPerTile + lane] = upto ? 31 - __clz(upto) : 0;
         }
         const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
         const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
