@@ -223,6 +223,37 @@ int lazy_device_status(void* stream, uint32_t* status);
 /* Thread-local message for the last non-zero return code of this thread. */
 const char* lazy_last_error(void);
 
+/* ------------------------------------------------------------------------------------------
+ * Document cache manager (host only).  [NOTE] 研究背景与动机 (核心矛盾: with a Zipf document
+ * popularity, D possible positions and a budget of C entries, a position-free cache holds the
+ * top C documents while a position-aware one holds only floor(C/D) of them) and 关键设计
+ * (Deferred Positional Encoding: one physical copy serves every position).
+ * Decides which documents' pages are resident in a pool of num_pages pages ([0, num_pages) of
+ * the K/V caches).  position_aware = 0: one entry per document (this library's cache);
+ * position_aware = 1: one entry per (document, position) variant (the design the pages
+ * compare against; for simulation).  Least-recently-used eviction among entries no batch
+ * holds.  The handle is host memory owned by the caller (create / destroy); not thread-safe.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct lazy_doc_cache lazy_doc_cache;
+/* NULL on error (num_pages outside [1, 2^24]; lazy_last_error says why). */
+lazy_doc_cache* lazy_doc_cache_create(int num_pages, int position_aware);
+void lazy_doc_cache_destroy(lazy_doc_cache* cache);
+/* Look up without changing recency or pins: returns the entry's page count (its page ids copied
+ * to pages_out (host) if not NULL and max_pages is large enough), 0 if not resident, < 0 on an
+ * argument error.  `pos` is ignored by a position-agnostic cache. */
+int lazy_doc_cache_lookup(lazy_doc_cache* cache, int doc, int pos, int32_t* pages_out, int max_pages);
+/* Hold document `doc` (at position `pos`) for a batch: on a hit (*hit = 1) copies its n_pages
+ * page ids to pages_out (host); on a miss (*hit = 0) evicts unheld least-recently-used entries
+ * until n_pages pages are free and assigns them (the caller then writes the document there, e.g.
+ * with lazy_kv_write at local positions).  Either way the entry is pinned until
+ * lazy_doc_cache_release.  LAZY_ERANGE if held entries leave no room; LAZY_EINVAL on bad
+ * arguments or a cached entry of another size. */
+int lazy_doc_cache_acquire(lazy_doc_cache* cache, int doc, int pos, int n_pages, int32_t* pages_out, int* hit);
+int lazy_doc_cache_release(lazy_doc_cache* cache, int doc, int pos);
+/* Counters since creation (any pointer may be NULL). */
+int lazy_doc_cache_stats(const lazy_doc_cache* cache, long long* hits, long long* misses, long long* evictions,
+                         int* entries, int* free_pages);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int lazy_version(void);
 

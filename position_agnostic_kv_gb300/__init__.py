@@ -16,7 +16,7 @@ import os
 
 import numpy as np
 
-__all__ = ["LIB_PATH", "lib", "PosCfg", "LazyError", "POS_ROPE", "POS_YARN", "POS_ALIBI",
+__all__ = ["LIB_PATH", "lib", "PosCfg", "LazyError", "DocCache", "POS_ROPE", "POS_YARN", "POS_ALIBI",
            "POS_NONE", "PHASE_DECODE", "PHASE_PREFILL", "EXPORTED_SYMBOLS", "build_doc_meta",
            "build_rope_table", "kv_write", "attn_decode", "attn_decode_noalloc", "attn_prefill", "workspace_size",
            "device_status", "pos_cfg_from"]
@@ -26,7 +26,9 @@ POS_ROPE, POS_YARN, POS_ALIBI, POS_NONE = 0, 1, 2, 3
 PHASE_DECODE, PHASE_PREFILL = 0, 1
 EXPORTED_SYMBOLS = ("lazy_build_doc_meta", "lazy_build_rope_table", "lazy_kv_write",
                     "lazy_attn_decode", "lazy_attn_decode_noalloc", "lazy_attn_prefill", "lazy_workspace_size",
-                    "lazy_device_status", "lazy_last_error", "lazy_version")
+                    "lazy_device_status", "lazy_last_error", "lazy_version", "lazy_doc_cache_create",
+                    "lazy_doc_cache_destroy", "lazy_doc_cache_lookup", "lazy_doc_cache_acquire",
+                    "lazy_doc_cache_release", "lazy_doc_cache_stats")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
@@ -71,6 +73,20 @@ for _name, _args in _sig.items():
     _f.restype = _I
 lib.lazy_workspace_size.restype = _SZ
 lib.lazy_last_error.restype = ctypes.c_char_p
+_LL = ctypes.POINTER(ctypes.c_longlong)
+_IP = ctypes.POINTER(ctypes.c_int)
+lib.lazy_doc_cache_create.argtypes = [_I, _I]
+lib.lazy_doc_cache_create.restype = _P
+lib.lazy_doc_cache_destroy.argtypes = [_P]
+lib.lazy_doc_cache_destroy.restype = None
+lib.lazy_doc_cache_lookup.argtypes = [_P, _I, _I, _P, _I]
+lib.lazy_doc_cache_lookup.restype = _I
+lib.lazy_doc_cache_acquire.argtypes = [_P, _I, _I, _I, _P, _IP]
+lib.lazy_doc_cache_acquire.restype = _I
+lib.lazy_doc_cache_release.argtypes = [_P, _I, _I]
+lib.lazy_doc_cache_release.restype = _I
+lib.lazy_doc_cache_stats.argtypes = [_P, _LL, _LL, _LL, _IP, _IP]
+lib.lazy_doc_cache_stats.restype = _I
 
 
 def _check(rc: int, what: str):
@@ -253,3 +269,56 @@ def device_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(lib.lazy_device_status(_stream(stream), ctypes.byref(v)), "lazy_device_status")
     return int(v.value)
+
+
+# ------------------------------------------------------------------ document cache manager
+class DocCache:
+    """Host document cache manager over a pool of ``num_pages`` pages (``lazy_doc_cache_*``):
+    one entry per document (position-agnostic, this library's cache) or, with
+    ``position_aware=True``, one per (document, position) variant (for comparison)."""
+
+    def __init__(self, num_pages: int, position_aware: bool = False):
+        self._h = lib.lazy_doc_cache_create(int(num_pages), int(bool(position_aware)))
+        if not self._h:
+            raise LazyError(f"lazy_doc_cache_create failed: {lib.lazy_last_error().decode(errors='replace')}")
+        self.num_pages = int(num_pages)
+        self.position_aware = bool(position_aware)
+
+    def close(self):
+        if self._h:
+            lib.lazy_doc_cache_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def lookup(self, doc: int, pos: int = 0):
+        """Page ids of the resident entry (a numpy int32 array) or None; no recency change."""
+        n = lib.lazy_doc_cache_lookup(self._h, int(doc), int(pos), None, 0)
+        if n < 0:
+            _check(n, "lazy_doc_cache_lookup")
+        if n == 0:
+            return None
+        out = np.zeros(n, np.int32)
+        _check(0 if lib.lazy_doc_cache_lookup(self._h, int(doc), int(pos), out.ctypes.data, n) == n else -1,
+               "lazy_doc_cache_lookup")
+        return out
+
+    def acquire(self, doc: int, n_pages: int, pos: int = 0):
+        """Hold the entry for a batch: (pages int32 array, hit bool).  On a miss the pages are
+        newly assigned and the caller writes the document into them."""
+        out = np.zeros(int(n_pages), np.int32)
+        hit = ctypes.c_int(0)
+        _check(lib.lazy_doc_cache_acquire(self._h, int(doc), int(pos), int(n_pages), out.ctypes.data,
+                                          ctypes.byref(hit)), "lazy_doc_cache_acquire")
+        return out, bool(hit.value)
+
+    def release(self, doc: int, pos: int = 0):
+        _check(lib.lazy_doc_cache_release(self._h, int(doc), int(pos)), "lazy_doc_cache_release")
+
+    def stats(self) -> dict:
+        h, m, e = ctypes.c_longlong(), ctypes.c_longlong(), ctypes.c_longlong()
+        n, f = ctypes.c_int(), ctypes.c_int()
+        _check(lib.lazy_doc_cache_stats(self._h, ctypes.byref(h), ctypes.byref(m), ctypes.byref(e),
+                                        ctypes.byref(n), ctypes.byref(f)), "lazy_doc_cache_stats")
+        return {"hits": h.value, "misses": m.value, "evictions": e.value, "entries": n.value,
+                "free_pages": f.value}
