@@ -157,23 +157,29 @@ def softmax_scale(pos: dict, head_dim: int) -> float:
     return s
 
 
-def rotate(x: np.ndarray, pos, inv_freq: np.ndarray) -> np.ndarray:
-    """R_pos x for half-split RoPE, fp64.
+def rotate(x: np.ndarray, pos, inv_freq: np.ndarray, interleaved: bool = False) -> np.ndarray:
+    """R_pos x for RoPE over the first d = 2 * len(inv_freq) dimensions, fp64.
 
-    x has shape [..., D]; pos broadcasts against x[..., 0].  Pair i is (x_i, x_{i+d/2}) with
-    angle pos * theta_i, and the rotation is the one the pages print for the deferred step
+    x has shape [..., D]; pos broadcasts against x[..., 0].  Pair i is (x_i, x_{i+d/2})
+    (half-split, the form the pages use) or (x_{2i}, x_{2i+1}) (interleaved, GPT-J style; the
+    pages list the other RoPE variants as metadata-only changes, [NOTE] 通用性), with angle
+    pos * theta_i, and the rotation is the one the pages print for the deferred step
     ([NOTE] 关键设计 / Deferred Positional Encoding): x'_1 = x_1 cos - x_2 sin,
-    x'_2 = x_1 sin + x_2 cos.  Dimensions beyond the rotary dimension pass through.
+    x'_2 = x_1 sin + x_2 cos.  Dimensions beyond d pass through (partial rotary_dim).
     """
     x = np.asarray(x, dtype=np.float64)
     half = inv_freq.shape[0]
     rd = 2 * half
     ang = np.asarray(pos, dtype=np.float64)[..., None] * inv_freq
     c, s = np.cos(ang), np.sin(ang)
-    x1, x2 = x[..., :half], x[..., half:rd]
+    if interleaved:
+        i1, i2 = np.arange(0, rd, 2), np.arange(1, rd, 2)
+    else:
+        i1, i2 = np.arange(half), np.arange(half, rd)
+    x1, x2 = x[..., i1], x[..., i2]
     out = x.copy()
-    out[..., :half] = x1 * c - x2 * s
-    out[..., half:rd] = x1 * s + x2 * c
+    out[..., i1] = x1 * c - x2 * s
+    out[..., i2] = x1 * s + x2 * c
     return out
 
 
@@ -265,7 +271,7 @@ def kv_write(k_raw_bits, v_bits, slot, local_pos, pos: dict, k_cache_bits, v_cac
     inv = pos_inv_freq(pos)
     k = bf16_bits_to_f64(k_raw_bits)
     if inv is not None:
-        k = rotate(k, np.asarray(local_pos)[:, None], inv)
+        k = rotate(k, np.asarray(local_pos)[:, None], inv, pos.get("interleaved", False))
     kb = f64_to_bf16_bits(round_to_bf16(k))
     slot = np.asarray(slot, dtype=np.int64)
     page, row = slot // PAGE, slot % PAGE
@@ -361,8 +367,8 @@ def attend_paged(q_raw, m, meta_row, n_blocks, k_cache_bits, v_cache_bits, pos: 
     k, v, delta, p = gather_request(meta_row, n_blocks, k_cache_bits, v_cache_bits)
     m = np.asarray(m, dtype=np.int64)
     if inv is not None:
-        k = rotate(k, delta[:, None], inv)
-        q = rotate(q, m[:, None], inv)
+        k = rotate(k, delta[:, None], inv, pos.get("interleaved", False))
+        q = rotate(q, m[:, None], inv, pos.get("interleaved", False))
     return softmax_attention(q, m, k, v, p, scale, slopes)
 
 
@@ -423,8 +429,8 @@ def materialized_attention(segments, q_raw, m, pos: dict, scale=None):
     p = np.arange(k.shape[0], dtype=np.int64)
     m = np.asarray(m, dtype=np.int64)
     if inv is not None:
-        k = rotate(k, p[:, None], inv)
-        q = rotate(q, m[:, None], inv)
+        k = rotate(k, p[:, None], inv, pos.get("interleaved", False))
+        q = rotate(q, m[:, None], inv, pos.get("interleaved", False))
     return softmax_attention(q, m, k, v, p, scale, slopes)
 
 
@@ -444,6 +450,8 @@ def full_recompute_loops(segments, q_raw, m, pos: dict, scale=None):
     Hkv = keys[0][1].shape[0]
     G = Hq // Hkv
 
+    inter = pos.get("interleaved", False)
+
     def rot(vec, position):
         if inv is None:
             return vec.copy()
@@ -452,8 +460,9 @@ def full_recompute_loops(segments, q_raw, m, pos: dict, scale=None):
         for i in range(half):
             a = position * inv[i]
             c, s = math.cos(a), math.sin(a)
-            out[i] = vec[i] * c - vec[i + half] * s
-            out[i + half] = vec[i] * s + vec[i + half] * c
+            j1, j2 = (2 * i, 2 * i + 1) if inter else (i, i + half)
+            out[j1] = vec[j1] * c - vec[j2] * s
+            out[j2] = vec[j1] * s + vec[j2] * c
         return out
 
     out = np.zeros((M, Hq, D))

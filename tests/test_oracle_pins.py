@@ -54,6 +54,43 @@ def test_rotation_equals_complex_multiplication():
     np.testing.assert_allclose(got[:, d // 2:], zr.imag, atol=1e-9)
 
 
+def test_interleaved_rotation_equals_complex_multiplication():
+    """Interleaved (GPT-J) RoPE is z_i * exp(i p theta_i) on z_i = x_{2i} + i x_{2i+1}; with a
+    partial rotary dimension d < D the dimensions from d on are untouched."""
+    D, d = 64, 32
+    inv = lo.rope_inv_freq(d, 1e4)
+    x = RNG.standard_normal((5, D))
+    p = np.array([0, 1, 17, 1000, 123456])
+    z = x[:, 0:d:2] + 1j * x[:, 1:d:2]
+    zr = z * np.exp(1j * p[:, None] * inv[None, :])
+    got = lo.rotate(x, p, inv, interleaved=True)
+    np.testing.assert_allclose(got[:, 0:d:2], zr.real, atol=1e-9)
+    np.testing.assert_allclose(got[:, 1:d:2], zr.imag, atol=1e-9)
+    np.testing.assert_array_equal(got[:, d:], x[:, d:])
+    half = lo.rotate(x, p, inv)
+    zh = x[:, : d // 2] + 1j * x[:, d // 2: d]
+    np.testing.assert_allclose(half[:, : d // 2] + 1j * half[:, d // 2: d],
+                               zh * np.exp(1j * p[:, None] * inv[None, :]), atol=1e-9)
+    np.testing.assert_array_equal(half[:, d:], x[:, d:])
+
+
+@pytest.mark.parametrize("inter", [False, True])
+def test_relative_identity_partial_and_interleaved(inter):
+    """(R_m q)^T (R_n k) = q^T R_{n-m} k also for interleaved pairs and partial rotary_dim (the
+    unrotated tail contributes its plain dot product); theta_i uses the rotary dimension."""
+    D, d = 128, 64
+    inv = lo.rope_inv_freq(d, 5e5)
+    assert abs(inv[d // 4] - 1.0 / math.sqrt(5e5)) < 1e-17
+    for _ in range(20):
+        q, k = RNG.standard_normal(D), RNG.standard_normal(D)
+        m, n = RNG.integers(0, 200_000, size=2)
+        lhs = lo.rotate(q, m, inv, inter) @ lo.rotate(k, n, inv, inter)
+        rhs = q @ lo.rotate(k, n - m, inv, inter)
+        assert abs(lhs - rhs) <= 1e-9 * (np.linalg.norm(q) * np.linalg.norm(k))
+        np.testing.assert_allclose(lo.rotate(lo.rotate(k, m, inv, inter), n, inv, inter),
+                                   lo.rotate(k, m + n, inv, inter), atol=1e-9)
+
+
 def test_inv_freq_special_values():
     """theta_0 = 1 and theta_{d/4} = base^(-1/2); strictly decreasing."""
     t = lo.rope_inv_freq(64, 1e4)
@@ -218,7 +255,7 @@ def _exact_caches(w):
     def put(k, v, slot, lp):
         kk = lo.bf16_bits_to_f64(k)
         if inv is not None:
-            kk = lo.rotate(kk, np.asarray(lp)[:, None], inv)
+            kk = lo.rotate(kk, np.asarray(lp)[:, None], inv, w.pos.interleaved)
         kc[slot // 16, :, slot % 16] = kk
         vc[slot // 16, :, slot % 16] = lo.bf16_bits_to_f64(v)
     for i in range(len(w.inst_doc)):
@@ -237,7 +274,7 @@ EDGE_CASES = [
 ]
 
 
-@pytest.mark.parametrize("kind", ["rope", "yarn", "alibi"])
+@pytest.mark.parametrize("kind", ["rope", "yarn", "alibi", "rope_partial", "rope_interleaved"])
 @pytest.mark.parametrize("case", range(len(EDGE_CASES)))
 def test_paged_oracle_equals_brute_force_loops(case, kind):
     """The paged route (block words, R_Delta on local-rotated K) equals an explicit-loop full
@@ -245,6 +282,8 @@ def test_paged_oracle_equals_brute_force_loops(case, kind):
     [GIST] Equivalenza Matematica), for prefill rows and for the decode rows."""
     doc_len, req_docs, Hq, Hkv, D, q_len, n_dec = EDGE_CASES[case]
     pos = {"rope": PosCfg("rope", 1e4, D),
+           "rope_partial": PosCfg("rope", 1e4, D // 2),
+           "rope_interleaved": PosCfg("yarn", 1e4, D, yarn_factor=4.0, yarn_orig_ctx=32, interleaved=True),
            "yarn": PosCfg("yarn", 5e5, D, yarn_factor=8.0, yarn_orig_ctx=64),
            "alibi": PosCfg("alibi", rotary_dim=D,
                            alibi_slopes=lo.alibi_slopes(Hq).astype(np.float32))}[kind]
@@ -266,7 +305,7 @@ def test_paged_oracle_equals_brute_force_loops(case, kind):
         qd, kd, vd, slot, lp = w.decode_tokens(t)
         kk = lo.bf16_bits_to_f64(kd)
         if inv is not None:
-            kk = lo.rotate(kk, lp[:, None], inv)
+            kk = lo.rotate(kk, lp[:, None], inv, w.pos.interleaved)
         kc[slot // 16, :, slot % 16] = kk
         vc[slot // 16, :, slot % 16] = lo.bf16_bits_to_f64(vd)
         sl = q_start + w.q_len + t + 1

@@ -87,12 +87,13 @@ class PosCfg:
     yarn_beta_fast: float = 32.0
     yarn_beta_slow: float = 1.0
     alibi_slopes: np.ndarray | None = None   # float32 [Hq], ALiBi only
+    interleaved: bool = False                # pairs (x_2i, x_2i+1) instead of (x_i, x_i+d/2)
 
     def as_dict(self) -> dict:
         return dict(kind=self.kind, rope_theta=self.rope_theta, rotary_dim=self.rotary_dim,
                     yarn_factor=self.yarn_factor, yarn_orig_ctx=self.yarn_orig_ctx,
                     yarn_beta_fast=self.yarn_beta_fast, yarn_beta_slow=self.yarn_beta_slow,
-                    alibi_slopes=self.alibi_slopes)
+                    alibi_slopes=self.alibi_slopes, interleaved=self.interleaved)
 
 
 @dataclass
