@@ -24,7 +24,8 @@
  *     Argument errors are detected on the host before anything is launched.  Errors found
  *     by a kernel (an out-of-range page or slot, a wait that ran out) set bits of the device
  *     status word and the offending element is skipped; no kernel traps or asserts.
- *   - Head dims supported: D in {64, 128} with rotary_dim == D.  Hq % Hkv == 0.
+ *   - Head dims supported: D in {64, 128}; rotary_dim a multiple of 16 in [16, D] (RoPE and
+ *     YaRN).  Hq % Hkv == 0.
  */
 #ifndef LAZYKV_H
 #define LAZYKV_H
@@ -53,7 +54,8 @@ extern "C" {
 
 /* Positional encodings ([NOTE] 通用性: RoPE variants and ALiBi change only metadata). */
 enum {
-  LAZY_POS_ROPE = 0,  /* half-split RoPE, theta_i = rope_theta^(-2i/rotary_dim)          */
+  LAZY_POS_ROPE = 0,  /* RoPE, theta_i = rope_theta^(-2i/rotary_dim); half-split pairs
+                         (x_i, x_{i+rotary_dim/2}) or interleaved (x_2i, x_2i+1)          */
   LAZY_POS_YARN = 1,  /* YaRN-scaled RoPE frequencies (YaRN paper's ramp) + mscale^2     */
   LAZY_POS_ALIBI = 2, /* no rotation; logit += -alibi_slopes[h] * (m - p)                */
   LAZY_POS_NONE = 3   /* no positional work at all: the "Delta = 0" twin used to time the
@@ -62,7 +64,9 @@ enum {
 
 /*
  * Positional configuration, read on the host at call time (by value semantics).
- *   rope_theta, rotary_dim          RoPE base and rotated width (rotary_dim == D).
+ *   rope_theta, rotary_dim          RoPE base and rotated width: the first rotary_dim
+ *                                   dimensions of every head are rotated, the rest pass
+ *                                   through (a multiple of 16 in [16, D]).
  *   yarn_factor, yarn_orig_ctx,     YaRN scale s, original context L0, ramp bounds
  *   yarn_beta_fast, yarn_beta_slow  (defaults 32 and 1 when given as 0).
  *   alibi_slopes                    (device) float [Hq]; ALiBi only.
@@ -70,6 +74,9 @@ enum {
  *                                   lazy_build_rope_table (cos in the first half of a row,
  *                                   sin in the second), or NULL: compute cos/sin on the fly.
  *   max_pos                         rows of cos_sin.
+ *   interleaved                     0: half-split pairs (x_i, x_{i + rotary_dim/2}) (NeoX /
+ *                                   Llama); 1: adjacent pairs (x_2i, x_2i+1) (GPT-J).  The
+ *                                   pages treat RoPE variants as metadata ([NOTE] 通用性).
  */
 typedef struct lazy_pos_cfg {
   int32_t kind;
@@ -82,6 +89,7 @@ typedef struct lazy_pos_cfg {
   const float* alibi_slopes;
   const float* cos_sin;
   int32_t max_pos;
+  int32_t interleaved;
 } lazy_pos_cfg;
 
 /*

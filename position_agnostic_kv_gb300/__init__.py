@@ -46,7 +46,8 @@ class PosCfg(ctypes.Structure):
                 ("rope_theta", ctypes.c_float), ("yarn_factor", ctypes.c_float),
                 ("yarn_orig_ctx", ctypes.c_int32), ("yarn_beta_fast", ctypes.c_float),
                 ("yarn_beta_slow", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
-                ("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32)]
+                ("cos_sin", ctypes.c_void_p), ("max_pos", ctypes.c_int32),
+                ("interleaved", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -120,13 +121,16 @@ def _stream(stream):
 
 def pos_cfg_from(kind: str, head_dim: int, rope_theta: float = 1e4, yarn_factor: float = 1.0,
                  yarn_orig_ctx: int = 0, yarn_beta_fast: float = 32.0,
-                 yarn_beta_slow: float = 1.0, alibi_slopes=None, cos_sin=None) -> PosCfg:
-    """Build a ``PosCfg`` (device tensors for slopes / table are referenced, not copied)."""
+                 yarn_beta_slow: float = 1.0, alibi_slopes=None, cos_sin=None,
+                 rotary_dim: int | None = None, interleaved: bool = False) -> PosCfg:
+    """Build a ``PosCfg`` (device tensors for slopes / table are referenced, not copied).
+    ``rotary_dim`` defaults to ``head_dim``; ``interleaved`` selects (x_2i, x_2i+1) pairs."""
     import torch
     kinds = {"rope": POS_ROPE, "yarn": POS_YARN, "alibi": POS_ALIBI, "none": POS_NONE}
     c = PosCfg()
     c.kind = kinds[kind]
-    c.rotary_dim = head_dim
+    c.rotary_dim = head_dim if rotary_dim is None else int(rotary_dim)
+    c.interleaved = int(bool(interleaved))
     c.rope_theta = rope_theta
     c.yarn_factor = yarn_factor
     c.yarn_orig_ctx = yarn_orig_ctx

@@ -40,7 +40,8 @@ enum PosKind : int { kRope = LAZY_POS_ROPE, kYarn = LAZY_POS_YARN, kAlibi = LAZY
 
 struct PosParams {
   int kind;              // PosKind
-  int rotary_dim;
+  int rotary_dim;        // rotated dimensions (a multiple of 16, <= D); the rest pass through
+  int interleaved;       // pairs (2i, 2i+1) instead of (i, i + rotary_dim/2)
   float scale_log2;      // softmax scale * log2(e): logits are kept in base-2 units
   const float* slopes;   // ALiBi slopes [Hq] (device) or null
   const float* table;    // cos/sin table [max_pos][rotary_dim] (device) or null

@@ -87,15 +87,17 @@ int prepare_pos(const lazy_pos_cfg* cfg, int Hq, int D, float scale, PosParams* 
   out->slopes = cfg->alibi_slopes;
   out->table = cfg->cos_sin;
   out->max_pos = cfg->cos_sin ? cfg->max_pos : 0;
+  out->interleaved = cfg->interleaved != 0;
   if (cfg->kind < LAZY_POS_ROPE || cfg->kind > LAZY_POS_NONE)
     return fail(LAZY_EINVAL, "unknown positional kind %d", cfg->kind);
   const bool rotary = cfg->kind == LAZY_POS_ROPE || cfg->kind == LAZY_POS_YARN;
   double s = 1.0 / std::sqrt(double(D));
   if (rotary) {
-    if (cfg->rotary_dim != D)
-      return fail(LAZY_EINVAL, "rotary_dim (%d) must equal head_dim (%d)", cfg->rotary_dim, D);
+    const int rd = cfg->rotary_dim;
+    if (rd < 16 || rd > D || rd % 16)
+      return fail(LAZY_EINVAL, "rotary_dim (%d) must be a multiple of 16 in [16, head_dim = %d]", rd, D);
     if (!(cfg->rope_theta > 1.0f)) return fail(LAZY_EINVAL, "rope_theta must be > 1");
-    const int half = D / 2;
+    const int half = rd / 2;
     const double two_pi = 6.283185307179586476925286766559;
     double factor = cfg->yarn_factor, bf = cfg->yarn_beta_fast, bs = cfg->yarn_beta_slow;
     if (cfg->kind == LAZY_POS_YARN) {
@@ -106,7 +108,7 @@ int prepare_pos(const lazy_pos_cfg* cfg, int Hq, int D, float scale, PosParams* 
       if (!(bf > bs)) return fail(LAZY_EINVAL, "YaRN needs beta_fast > beta_slow");
     }
     for (int i = 0; i < half; ++i) {
-      double theta = std::pow(double(cfg->rope_theta), -2.0 * i / double(D));
+      double theta = std::pow(double(cfg->rope_theta), -2.0 * i / double(rd));
       if (cfg->kind == LAZY_POS_YARN) {
         // NTK-by-parts ramp of the YaRN paper: gamma = clamp((L0/lambda - b_slow)/(b_fast - b_slow))
         const double ratio = double(cfg->yarn_orig_ctx) * theta / two_pi;  // L0 / lambda_i

@@ -343,54 +343,79 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int m_row = valid ? mbase + token : -1;
     {
       const uint32_t sQ = sQ0 + uint32_t(qt * L::QTILE);
-      float x[D];
-      if (valid) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)(q0 + token) * a.Hq + h) * D);
+      // The raw row is staged in this thread's own row of the Q tile (bf16, swizzled), then
+      // rotated and scaled chunk by chunk in place, so a rotation partner at a run-time offset
+      // (rotary_dim / 2) needs no register indexing.
+      auto qaddr = [&](int k) { return sQ + uint32_t((k >> 3) * L::BLK) + swz(r, k & 7); };
+      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((size_t)(q0 + token) * a.Hq + h) * D);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 u = src[c];
-          x[c * 8 + 0] = bf_lo(u.x); x[c * 8 + 1] = bf_hi(u.x);
-          x[c * 8 + 2] = bf_lo(u.y); x[c * 8 + 3] = bf_hi(u.y);
-          x[c * 8 + 4] = bf_lo(u.z); x[c * 8 + 5] = bf_hi(u.z);
-          x[c * 8 + 6] = bf_lo(u.w); x[c * 8 + 7] = bf_hi(u.w);
-        }
-        if constexpr (kRotate) {
-          const uint32_t m = uint32_t(m_row);
-          const bool tab = a.pos.table != nullptr && int(m) < a.pos.max_pos;
+      for (int k = 0; k < D / 8; ++k) st_shared_v4(qaddr(k), valid ? src[k] : make_uint4(0, 0, 0, 0));
+      const float sc = a.pos.scale_log2;
+      auto pack = [&](const float (&y)[8]) {
+        if constexpr (kQkF16)
+          return make_uint4(f2_to_h2(y[0] * sc, y[1] * sc), f2_to_h2(y[2] * sc, y[3] * sc),
+                            f2_to_h2(y[4] * sc, y[5] * sc), f2_to_h2(y[6] * sc, y[7] * sc));
+        else
+          return make_uint4(f2_to_bf2(y[0] * sc, y[1] * sc), f2_to_bf2(y[2] * sc, y[3] * sc),
+                            f2_to_bf2(y[4] * sc, y[5] * sc), f2_to_bf2(y[6] * sc, y[7] * sc));
+      };
+      auto unpack = [](uint4 u, float (&y)[8]) {
+        y[0] = bf_lo(u.x); y[1] = bf_hi(u.x); y[2] = bf_lo(u.y); y[3] = bf_hi(u.y);
+        y[4] = bf_lo(u.z); y[5] = bf_hi(u.z); y[6] = bf_lo(u.w); y[7] = bf_hi(u.w);
+      };
+      int done = 0;  // chunks [0, done) already written in their final form
+      if constexpr (kRotate) {
+        const uint32_t m = uint32_t(m_row < 0 ? 0 : m_row);
+        const int rd = a.pos.rotary_dim, hr = rd / 2;
+        const bool tab = a.pos.table != nullptr && int(m) < a.pos.max_pos;
+        auto csf = [&](int i, float& sn, float& co) {
+          if (tab) {
+            co = a.pos.table[(size_t)m * rd + i];
+            sn = a.pos.table[(size_t)m * rd + hr + i];
+          } else {
+            turn_sincos(m, turns[i], sn, co);
+          }
+        };
+        if (!a.pos.interleaved) {
+#pragma unroll 1
+          for (int c = 0; c < hr / 8; ++c) {  // chunk c against its partner c + hr/8
+            float x1[8], x2[8];
+            unpack(ld_shared_v4(qaddr(c)), x1);
+            unpack(ld_shared_v4(qaddr(c + hr / 8)), x2);
+            float y1[8], y2[8];
 #pragma unroll
-          for (int i = 0; i < D / 2; ++i) {
-            float sn, co;
-            if (tab) {
-              co = a.pos.table[(size_t)m * D + i];
-              sn = a.pos.table[(size_t)m * D + D / 2 + i];
-            } else {
-              turn_sincos(m, turns[i], sn, co);
+            for (int e = 0; e < 8; ++e) {
+              float sn, co;
+              csf(c * 8 + e, sn, co);
+              y1[e] = x1[e] * co - x2[e] * sn;
+              y2[e] = x1[e] * sn + x2[e] * co;
             }
-            const float x1 = x[i], x2 = x[i + D / 2];
-            x[i] = x1 * co - x2 * sn;
-            x[i + D / 2] = x1 * sn + x2 * co;
+            st_shared_v4(qaddr(c), pack(y1));
+            st_shared_v4(qaddr(c + hr / 8), pack(y2));
+          }
+        } else {
+#pragma unroll 1
+          for (int k = 0; k < rd / 8; ++k) {  // adjacent pairs (2i, 2i+1), i = 4k .. 4k+3
+            float x[8], y[8];
+            unpack(ld_shared_v4(qaddr(k)), x);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              float sn, co;
+              csf(k * 4 + w, sn, co);
+              y[2 * w] = x[2 * w] * co - x[2 * w + 1] * sn;
+              y[2 * w + 1] = x[2 * w] * sn + x[2 * w + 1] * co;
+            }
+            st_shared_v4(qaddr(k), pack(y));
           }
         }
-#pragma unroll
-        for (int i = 0; i < D; ++i) x[i] *= a.pos.scale_log2;
-      } else {
-#pragma unroll
-        for (int i = 0; i < D; ++i) x[i] = 0.f;
+        done = rd / 8;
       }
-#pragma unroll
-      for (int cb = 0; cb < L::CB; ++cb)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float* y = x + cb * 64 + c * 8;
-          if constexpr (kQkF16)
-            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(r, c),
-                         make_uint4(f2_to_h2(y[0], y[1]), f2_to_h2(y[2], y[3]), f2_to_h2(y[4], y[5]),
-                                    f2_to_h2(y[6], y[7])));
-          else
-            st_shared_v4(sQ + uint32_t(cb * L::BLK) + swz(r, c),
-                         make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
-                                    f2_to_bf2(y[6], y[7])));
-        }
+#pragma unroll 1
+      for (int k = done; k < D / 8; ++k) {  // unrotated dimensions: scale and convert
+        float x[8];
+        unpack(ld_shared_v4(qaddr(k)), x);
+        st_shared_v4(qaddr(k), pack(x));
+      }
       fence_async_smem();
       mbar_arrive(BAR(B_Q_READY));
     }
@@ -550,27 +575,75 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         named_sync(1, 128);
         if (ok && t < pi.y) {
           const float4* c4 = cs4 + run_start * (D / 4);
+          const int rd = a.pos.rotary_dim;
+          if (rd == D && !a.pos.interleaved) {  // full half-split rotation (the common case)
 #pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            // pair i = c*8 + e: element i and its partner i + D/2 share the swizzled chunk slot
-            const uint32_t a1 = sK + swz(rt, c);
-            const uint32_t a2 = (D == 128) ? sK + uint32_t(L::BLK) + swz(rt, c) : sK + swz(rt, c + 4);
-            uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
-            uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
-            uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
+            for (int c = 0; c < D / 16; ++c) {
+              // pair i = c*8 + e: element i and its partner i + D/2 share the swizzled chunk slot
+              const uint32_t a1 = sK + swz(rt, c);
+              const uint32_t a2 = (D == 128) ? sK + uint32_t(L::BLK) + swz(rt, c) : sK + swz(rt, c + 4);
+              uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
+              uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
+              uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float4 cc = c4[c * 4 + w];  // pairs c*8 + 2w, c*8 + 2w + 1
-              const float2 cv = make_float2(cc.x, cc.y), sv = make_float2(cc.z, cc.w);
-              const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
-              const float2 t1 = __fmul2_rn(x2, sv), t2 = __fmul2_rn(x2, cv);
-              const float2 y1 = __ffma2_rn(x1, cv, make_float2(-t1.x, -t1.y));  // x1 c - x2 s
-              const float2 y2 = __ffma2_rn(x1, sv, t2);                          // x1 s + x2 c
-              p1[w] = f2_to_h2(y1.x, y1.y);
-              p2[w] = f2_to_h2(y2.x, y2.y);
+              for (int w = 0; w < 4; ++w) {
+                const float4 cc = c4[c * 4 + w];  // pairs c*8 + 2w, c*8 + 2w + 1
+                const float2 cv = make_float2(cc.x, cc.y), sv = make_float2(cc.z, cc.w);
+                const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
+                const float2 t1 = __fmul2_rn(x2, sv), t2 = __fmul2_rn(x2, cv);
+                const float2 y1 = __ffma2_rn(x1, cv, make_float2(-t1.x, -t1.y));  // x1 c - x2 s
+                const float2 y2 = __ffma2_rn(x1, sv, t2);                          // x1 s + x2 c
+                p1[w] = f2_to_h2(y1.x, y1.y);
+                p2[w] = f2_to_h2(y2.x, y2.y);
+              }
+              st_shared_v4(a1, u1);
+              st_shared_v4(a2, u2);
             }
-            st_shared_v4(a1, u1);
-            st_shared_v4(a2, u2);
+          } else {  // partial rotary_dim and / or interleaved pairs
+            auto kaddr = [&](int k) { return sK + uint32_t((k >> 3) * L::BLK) + swz(rt, k & 7); };
+            if (!a.pos.interleaved) {
+              const int hc = rd / 16;
+#pragma unroll 1
+              for (int c = 0; c < hc; ++c) {  // chunk c against its partner c + rotary_dim/16
+                const uint32_t a1 = kaddr(c), a2 = kaddr(c + hc);
+                uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
+                uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
+                uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const float4 cc = c4[c * 4 + w];
+                  const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
+                  p1[w] = f2_to_h2(x1.x * cc.x - x2.x * cc.z, x1.y * cc.y - x2.y * cc.w);
+                  p2[w] = f2_to_h2(x1.x * cc.z + x2.x * cc.x, x1.y * cc.w + x2.y * cc.y);
+                }
+                st_shared_v4(a1, u1);
+                st_shared_v4(a2, u2);
+              }
+            } else {
+#pragma unroll 1
+              for (int k = 0; k < rd / 8; ++k) {  // word w = (x_2i, x_2i+1), pair i = 4k + w
+                const uint32_t a1 = kaddr(k);
+                uint4 u = ld_shared_v4(a1);
+                uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const float4 cc = c4[2 * k + (w >> 1)];  // frequencies 2q, 2q+1 with q = i / 2
+                  const float co = (w & 1) ? cc.y : cc.x, sn = (w & 1) ? cc.w : cc.z;
+                  const float x0 = bf_lo(pw[w]), x1 = bf_hi(pw[w]);
+                  pw[w] = f2_to_h2(x0 * co - x1 * sn, x0 * sn + x1 * co);
+                }
+                st_shared_v4(a1, u);
+              }
+            }
+#pragma unroll 1
+            for (int k = rd / 8; k < D / 8; ++k) {  // unrotated tail: bf16 -> f16 (one MMA type)
+              const uint32_t a1 = kaddr(k);
+              uint4 u = ld_shared_v4(a1);
+              uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+              for (int w = 0; w < 4; ++w) pw[w] = f2_to_h2(bf_lo(pw[w]), bf_hi(pw[w]));
+              st_shared_v4(a1, u);
+            }
           }
         }
         fence_async_smem();

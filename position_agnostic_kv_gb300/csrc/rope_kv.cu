@@ -22,8 +22,23 @@ __global__ void rope_table_kernel(PosParams pos, int max_pos, float* __restrict_
   }
 }
 
-// One thread per (token, head, 8-pair chunk): reads k[c..c+8) and k[c+d/2..c+d/2+8), writes
-// the rotated pairs (fp32 math, one round to bf16) and copies v.  D/16 threads per (t, h).
+// cos / sin of frequency i at position j (table row j: cos of the rotary_dim/2 frequencies,
+// then their sin), or on the fly from exact turns.
+__device__ __forceinline__ void pos_cs(const PosParams& pos, uint32_t j, bool use_table, int i, float& s, float& c) {
+  if (use_table) {
+    c = pos.table[(long long)j * pos.rotary_dim + i];
+    s = pos.table[(long long)j * pos.rotary_dim + pos.rotary_dim / 2 + i];
+  } else {
+    turn_sincos(j, pos.turns[i], s, c);
+  }
+}
+
+// One thread per (token, head, pair of 16-byte chunks); D/16 threads per (t, h).  Half-split
+// RoPE: thread `part` < rotary_dim/16 rotates chunk `part` against its partner
+// `part + rotary_dim/16` (pairs (i, i + rotary_dim/2)); the other threads copy the unrotated
+// tail two chunks at a time.  Interleaved RoPE: thread `part` takes chunks 2 part and
+// 2 part + 1 and rotates the adjacent pairs of those below rotary_dim.  fp32 math, one
+// rounding to bf16; V is copied.
 template <int D, bool ROTATE>
 __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                                        const int32_t* __restrict__ slot,
@@ -45,33 +60,50 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
   const int page = sl / kPage, r = sl % kPage;
   const long long src = row * CH;
   const long long dst = (((long long)page * Hkv + h) * kPage + r) * CH;
-  const int c1 = part, c2 = part + CH / 2;  // chunk of the first half and its partner
+  const int hc = pos.rotary_dim / 16;  // half-split: rotated chunk pairs
+  const bool half_pair = ROTATE && !pos.interleaved && part < hc;
+  int c1 = 2 * part, c2 = 2 * part + 1;
+  if (ROTATE && !pos.interleaved) {
+    c1 = half_pair ? part : 2 * hc + 2 * (part - hc);
+    c2 = half_pair ? part + hc : c1 + 1;
+  }
   uint4 a = k[src + c1], b = k[src + c2];
   if (ROTATE) {
     const uint32_t j = uint32_t(local_pos[t]);
+    const bool use_table = pos.table != nullptr && int(j) < pos.max_pos;
     uint32_t* pa = reinterpret_cast<uint32_t*>(&a);
     uint32_t* pb = reinterpret_cast<uint32_t*>(&b);
-    const bool use_table = pos.table != nullptr && int(j) < pos.max_pos;
+    if (half_pair) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float x1[2] = {bf_lo(pa[w]), bf_hi(pa[w])};
-      float x2[2] = {bf_lo(pb[w]), bf_hi(pb[w])};
-      float y1[2], y2[2];
+      for (int w = 0; w < 4; ++w) {
+        float x1[2] = {bf_lo(pa[w]), bf_hi(pa[w])};
+        float x2[2] = {bf_lo(pb[w]), bf_hi(pb[w])};
+        float y1[2], y2[2];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int i = part * 8 + w * 2 + e;  // pair index
-        float s, c;
-        if (use_table) {
-          c = pos.table[(long long)j * D + i];
-          s = pos.table[(long long)j * D + D / 2 + i];
-        } else {
-          turn_sincos(j, pos.turns[i], s, c);
+        for (int e = 0; e < 2; ++e) {
+          float s, c;
+          pos_cs(pos, j, use_table, part * 8 + w * 2 + e, s, c);  // pair index
+          y1[e] = x1[e] * c - x2[e] * s;
+          y2[e] = x1[e] * s + x2[e] * c;
         }
-        y1[e] = x1[e] * c - x2[e] * s;
-        y2[e] = x1[e] * s + x2[e] * c;
+        pa[w] = f2_to_bf2(y1[0], y1[1]);
+        pb[w] = f2_to_bf2(y2[0], y2[1]);
       }
-      pa[w] = f2_to_bf2(y1[0], y1[1]);
-      pb[w] = f2_to_bf2(y2[0], y2[1]);
+    } else if (pos.interleaved) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int cc = q ? c2 : c1;
+        uint32_t* pw = q ? pb : pa;
+        if (cc < pos.rotary_dim / 8) {
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {  // word w = (x_2i, x_2i+1), pair i = 4 cc + w
+            float s, c;
+            pos_cs(pos, j, use_table, cc * 4 + w, s, c);
+            const float x0 = bf_lo(pw[w]), x1 = bf_hi(pw[w]);
+            pw[w] = f2_to_bf2(x0 * c - x1 * s, x0 * s + x1 * c);
+          }
+        }
+      }
     }
   }
   kc[dst + c1] = a;
@@ -90,7 +122,8 @@ extern "C" int lazy_build_rope_table(const lazy_pos_cfg* cfg, int max_pos, float
   if (!cfg || !out_table || max_pos <= 0) return fail(LAZY_EINVAL, "bad rope table arguments");
   if (cfg->kind != LAZY_POS_ROPE && cfg->kind != LAZY_POS_YARN)
     return fail(LAZY_EINVAL, "a cos/sin table exists only for RoPE and YaRN");
-  if (cfg->rotary_dim != 64 && cfg->rotary_dim != 128) return fail(LAZY_EINVAL, "rotary_dim must be 64 or 128");
+  if (cfg->rotary_dim < 16 || cfg->rotary_dim > 128 || cfg->rotary_dim % 16)
+    return fail(LAZY_EINVAL, "rotary_dim must be a multiple of 16 in [16, 128]");
   PosParams pos;
   lazy_pos_cfg c2 = *cfg;
   c2.cos_sin = nullptr;

@@ -57,18 +57,21 @@ class PagedBatch:
         if p.alibi_slopes is not None:
             self.slopes = torch.from_numpy(np.asarray(p.alibi_slopes, np.float32)).to(dev)
         self.table = None
+        rd = getattr(p, "rotary_dim", w.D) if kind in ("rope", "yarn") else w.D
+        inter = bool(getattr(p, "interleaved", False))
         self.cfg = pos_cfg_from(kind, w.D, rope_theta=p.rope_theta, yarn_factor=p.yarn_factor,
                                 yarn_orig_ctx=p.yarn_orig_ctx, yarn_beta_fast=p.yarn_beta_fast,
-                                yarn_beta_slow=p.yarn_beta_slow, alibi_slopes=self.slopes)
+                                yarn_beta_slow=p.yarn_beta_slow, alibi_slopes=self.slopes,
+                                rotary_dim=rd, interleaved=inter)
         if use_table and kind in ("rope", "yarn"):
             max_pos = int(self.q_start_h.max()) + int(np.max(w.q_len)) + w.n_decode + 1
-            self.table = torch.empty((max_pos, w.D), dtype=torch.float32, device=dev)
+            self.table = torch.empty((max_pos, rd), dtype=torch.float32, device=dev)
             build_rope_table(self.cfg, max_pos, self.table)
             self.cfg = pos_cfg_from(kind, w.D, rope_theta=p.rope_theta,
                                     yarn_factor=p.yarn_factor, yarn_orig_ctx=p.yarn_orig_ctx,
                                     yarn_beta_fast=p.yarn_beta_fast,
                                     yarn_beta_slow=p.yarn_beta_slow, alibi_slopes=self.slopes,
-                                    cos_sin=self.table)
+                                    cos_sin=self.table, rotary_dim=rd, interleaved=inter)
         self.max_blocks = w.max_blocks
         ws_dec = workspace_size(PHASE_DECODE, self.B, self.B, self.max_blocks, self.Hq, self.Hkv,
                                 self.D)

@@ -37,10 +37,11 @@ def _status_clean(lk):
 
 
 # ------------------------------------------------------------------ cos/sin table
-@pytest.mark.parametrize("kind", ["rope", "yarn"])
-def test_rope_table_matches_fp64(lk, kind):
+@pytest.mark.parametrize("kind,D", [("rope", 128), ("yarn", 128), ("rope", 48), ("yarn", 32)])
+def test_rope_table_matches_fp64(lk, kind, D):
+    """Table rows for full and partial rotary dimensions (D here is the rotary dimension)."""
     import torch
-    D, max_pos = 128, 40000
+    max_pos = 40000
     if kind == "rope":
         cfg = lk.pos_cfg_from("rope", D, rope_theta=5e5)
         inv = lo.rope_inv_freq(D, 5e5)
@@ -290,6 +291,39 @@ def test_cold_document_encode_then_reuse(lk, D, Hq, Hkv, L):
             (lo.bf16_bits_to_f64(kq), lo.bf16_bits_to_f64(vq))]
     ref2, _ = lo.materialized_attention(segs, lo.bf16_bits_to_f64(qq), pre_len + L + tq, pos.as_dict())
     assert_close(out2, ref2, "reuse of the cold-encoded document at offset 37")
+
+
+ROPE_VARIANTS = [  # D, Hq, Hkv, rotary_dim, interleaved, kind, table
+    (128, 8, 2, 64, False, "rope", False),
+    (128, 8, 2, 128, True, "rope", True),
+    (64, 4, 4, 32, True, "yarn", False),
+    (64, 16, 2, 48, False, "rope", True),
+    (128, 32, 1, 32, True, "rope", False),
+    (128, 32, 1, 96, False, "yarn", False),
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,rd,inter,kind,table", ROPE_VARIANTS)
+def test_rope_variants(lk, D, Hq, Hkv, rd, inter, kind, table):
+    """Interleaved (GPT-J) pairs and partial rotary_dim through every kernel: the written K
+    cache (one bf16 ulp of the oracle), the tensor-core prefill, the CUDA-core decode (G <= 8)
+    or the tensor-core decode (G >= 16), cos/sin on the fly or from the table."""
+    import torch
+    extra = dict(yarn_factor=8.0, yarn_orig_ctx=512) if kind == "yarn" else {}
+    pos = PosCfg(kind, 1e4, rd, interleaved=inter, **extra)
+    w = make_custom([1, 15, 16, 17, 333], [[4, 0, 2], [1, 3], [2, 4, 1, 0]], Hq, Hkv, D, pos,
+                    [3, 0, 17], 4, seed=D + Hq + rd)
+    _run_and_check(lk, w, [0, 1, 2], 4, {0, 3}, use_table=table)
+    pb = _batch(w, use_table=table)
+    pb.fill_documents()
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    kc, _ = oracle_caches_for(w, prefill=False)
+    gk, rk = lo.bf16_bits_to_f64(_bits(pb.k_cache)), lo.bf16_bits_to_f64(kc)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(rk), 2.0 ** -126))) - 7)
+    assert not (np.abs(gk - rk) > ulp + 6e-6).any()
+    # the dimensions beyond rotary_dim are stored unrotated (bit-exact copies)
+    np.testing.assert_array_equal(_bits(pb.k_cache)[..., rd:], kc[..., rd:])
 
 
 def test_sharpened_queries_separate_negative_controls(lk):
