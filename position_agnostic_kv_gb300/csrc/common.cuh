@@ -36,7 +36,8 @@ __host__ __device__ __forceinline__ uint32_t word_page(uint64_t w) { return uint
 //   turns of the angle p * theta_i (fixed-point phase accumulation, as in direct digital
 //   synthesis), so the angle is reduced without error for any p < 2^32 before sin/cos.
 // ------------------------------------------------------------------------------------------
-enum PosKind : int { kRope = LAZY_POS_ROPE, kYarn = LAZY_POS_YARN, kAlibi = LAZY_POS_ALIBI, kNone = LAZY_POS_NONE };
+enum PosKind : int { kRope = LAZY_POS_ROPE, kYarn = LAZY_POS_YARN, kAlibi = LAZY_POS_ALIBI, kNone = LAZY_POS_NONE,
+                     kRopeX = 16 /* kernel-internal: RoPE with partial rotary_dim or interleaved pairs */ };
 
 struct PosParams {
   int kind;              // PosKind

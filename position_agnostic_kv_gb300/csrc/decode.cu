@@ -214,48 +214,76 @@ __global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeA
     const uint32_t delta = word_delta(w);
     const int start = int(delta + kPage * word_pg(w));
 
-    if constexpr (POS == kRope || POS == kYarn) {
+    if constexpr (POS == kRope || POS == kYarn || POS == kRopeX) {
       if (delta != cur_delta) {  // document boundary: q_eff = R_{m - Delta} q_raw
         cur_delta = delta;
         const uint32_t dp = uint32_t(m) - delta;
-        // This lane's 8 columns c0..c0+7 are all of one kind (rotary_dim is a multiple of 16):
-        // the first or second element of half-split pairs (partner +-rd/2), adjacent
-        // interleaved pairs, or the unrotated tail.
-        const int rd = a.pos.rotary_dim, hr = rd / 2;
-        const bool inter = a.pos.interleaved != 0;
-        const int kind = c0 >= rd ? 3 : inter ? 2 : (c0 < hr ? 0 : 1);
-        const int f0 = kind == 2 ? c0 / 2 : (kind == 0 ? c0 : c0 - hr);  // first frequency
-        const bool tab = a.pos.table != nullptr && int(dp) < a.pos.max_pos;
-        float cs[8], sn[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int fi = f0 + (kind == 2 ? e / 2 : e);
-          if (kind == 3) {
-            cs[e] = 1.f;
-            sn[e] = 0.f;
-          } else if (tab) {
-            cs[e] = a.pos.table[(size_t)dp * rd + fi];
-            sn[e] = a.pos.table[(size_t)dp * rd + hr + fi];
-          } else {
-            turn_sincos(dp, a.pos.turns[fi], sn[e], cs[e]);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float* qh = qs + h * D;
-          float y[8];
+        if constexpr (POS == kRopeX) {
+          // Partial rotary_dim or interleaved pairs.  This lane's 8 columns c0..c0+7 are all of
+          // one kind (rotary_dim is a multiple of 16): the first or second element of
+          // half-split pairs (partner +-rd/2), adjacent interleaved pairs, or the unrotated tail.
+          const int rd = a.pos.rotary_dim, hr = rd / 2;
+          const bool inter = a.pos.interleaved != 0;
+          const int kind = c0 >= rd ? 3 : inter ? 2 : (c0 < hr ? 0 : 1);
+          const int f0 = kind == 2 ? c0 / 2 : (kind == 0 ? c0 : c0 - hr);  // first frequency
+          const bool tab = a.pos.table != nullptr && int(dp) < a.pos.max_pos;
+          float cs[8], sn[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float x = qh[c0 + e];
-            float v;
-            if (kind == 0) v = x * cs[e] - qh[c0 + e + hr] * sn[e];
-            else if (kind == 1) v = qh[c0 + e - hr] * sn[e] + x * cs[e];
-            else if (kind == 2) v = (e & 1) ? qh[c0 + e - 1] * sn[e] + x * cs[e] : x * cs[e] - qh[c0 + e + 1] * sn[e];
-            else v = x;
-            y[e] = v * a.pos.scale_log2;
+            const int fi = f0 + (kind == 2 ? e / 2 : e);
+            if (kind == 3) {
+              cs[e] = 1.f;
+              sn[e] = 0.f;
+            } else if (tab) {
+              cs[e] = a.pos.table[(size_t)dp * rd + fi];
+              sn[e] = a.pos.table[(size_t)dp * rd + hr + fi];
+            } else {
+              turn_sincos(dp, a.pos.turns[fi], sn[e], cs[e]);
+            }
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) qe[h][e] = make_float2(y[2 * e], y[2 * e + 1]);
+          for (int h = 0; h < G; ++h) {
+            const float* qh = qs + h * D;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float x = qh[c0 + e];
+              float v;
+              if (kind == 0) v = x * cs[e] - qh[c0 + e + hr] * sn[e];
+              else if (kind == 1) v = qh[c0 + e - hr] * sn[e] + x * cs[e];
+              else if (kind == 2) v = (e & 1) ? qh[c0 + e - 1] * sn[e] + x * cs[e] : x * cs[e] - qh[c0 + e + 1] * sn[e];
+              else v = x;
+              y[e] = v * a.pos.scale_log2;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qe[h][e] = make_float2(y[2 * e], y[2 * e + 1]);
+          }
+        } else {
+          // full-width half-split pairs (i, i + D/2)
+          const bool first_half = c0 < D / 2;
+          const int i0 = first_half ? c0 : c0 - D / 2;
+          const bool tab = a.pos.table != nullptr && int(dp) < a.pos.max_pos;
+          float cs[8], sn[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (tab) {
+              cs[e] = a.pos.table[(size_t)dp * D + i0 + e];
+              sn[e] = a.pos.table[(size_t)dp * D + D / 2 + i0 + e];
+            } else {
+              turn_sincos(dp, a.pos.turns[i0 + e], sn[e], cs[e]);
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float x1 = qs[h * D + i0 + e], x2 = qs[h * D + i0 + e + D / 2];
+              y[e] = (first_half ? (x1 * cs[e] - x2 * sn[e]) : (x1 * sn[e] + x2 * cs[e])) * a.pos.scale_log2;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qe[h][e] = make_float2(y[2 * e], y[2 * e + 1]);
+          }
         }
       }
     }
@@ -527,7 +555,9 @@ template <int D, int G, bool ROWS>
 static int launch_pos(const DecodeArgs& a, cudaStream_t st) {
   switch (a.pos.kind) {
     case kRope:
-    case kYarn: return launch_t<D, G, kRope, ROWS>(a, st);
+    case kYarn:
+      if (a.pos.rotary_dim != D || a.pos.interleaved) return launch_t<D, G, kRopeX, ROWS>(a, st);
+      return launch_t<D, G, kRope, ROWS>(a, st);
     case kAlibi: return launch_t<D, G, kAlibi, ROWS>(a, st);
     default: return launch_t<D, G, kNone, ROWS>(a, st);
   }
