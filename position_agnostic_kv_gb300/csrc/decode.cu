@@ -8,9 +8,10 @@
 //
 // Design (GB300):
 //  * One CTA = (query row, head group, KV split); 4 warps, each streaming a contiguous run of
-//    pages through its own ring of shared-memory stages filled by cp.async.bulk (one 4 KB
-//    K copy and one V copy per page and head, completed on an mbarrier).  No registers are
-//    spent on loads in flight, and every stage is in flight while earlier pages are used.
+//    pages through its own 2-stage ring of shared-memory stages filled by cp.async.bulk (one
+//    4 KB K copy and one V copy per page and head, completed on an mbarrier); 3 CTAs per SM.
+//    No registers are spent on loads in flight, and every stage is in flight while earlier
+//    pages are used.
 //  * A lane owns 8 columns (one 16-byte chunk) of a K/V row; D/8 lanes cover a row.  Per page
 //    every lane forms G x (rows per lane) partial dot products with packed fp32x2 FMAs, then a
 //    transposed butterfly over the row's lanes leaves each lane with complete scores.
@@ -78,7 +79,7 @@ struct DecLayout {
 };
 
 template <int D, int G, int POS, bool ROWS, int NST>
-__global__ void __launch_bounds__(kDecWarps * 32, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kernel(const DecodeArgs a) {
   using L = DecLayout<D, G, NST>;
   constexpr int LPR = L::LPR, RPI = L::RPI, RPL = L::RPL, V = L::V, E = L::E;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -479,7 +480,10 @@ __global__ void __launch_bounds__(D) merge_kernel(const float* __restrict__ part
 // ------------------------------------------------------------------------------------------
 // Host: split choice, workspace, dispatch
 // ------------------------------------------------------------------------------------------
-constexpr int kNst = 3;
+// Two stages per warp: 4 warps x 2 x 8 KB keeps a CTA at ~68 KB of shared memory and <= 168
+// registers (G <= 4), so three CTAs fit per SM; measured on GB300 against three stages at two
+// CTAs per SM: decode32k 1324 -> 1223 us, yarn8b 294 -> 267 us, rag8b unchanged.
+constexpr int kNst = 2;
 
 int decode_group(int Hq, int Hkv) {
   const int G = Hq / Hkv;
@@ -489,12 +493,12 @@ int decode_group(int Hq, int Hkv) {
 int choose_splits(int rows, int Hq, int Hkv, int max_blocks) {
   const int G = decode_group(Hq, Hkv);
   const long long units = (long long)rows * (Hq / G);
-  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // tuned wave unit (not occupancy)
-  // About 4 waves of resident CTAs, but at least 16 pages per warp: measured on GB300, long
-  // per-warp page runs beat more, shorter CTAs (every CTA pays a pipeline start-up and its
+  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // CTAs resident at once
+  // About 4 waves of resident CTAs, but runs of about 16 pages per warp: measured on GB300,
+  // long per-warp page runs beat more, shorter CTAs (every CTA pays a pipeline start-up and its
   // split partials), and a partial last wave costs little once there are several waves.
   const long long want = (4 * slots + units - 1) / units;
-  const int max_by_len = max(1, max_blocks / (kDecWarps * 16));
+  const int max_by_len = max(1, (max_blocks + kDecWarps * 16 - 1) / (kDecWarps * 16));
   long long s = want < max_by_len ? want : max_by_len;
   if (s < 1) s = 1;
   if (s > 64) s = 64;
