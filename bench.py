@@ -410,12 +410,12 @@ def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
                     if r >= 2:
                         ts.append(e0.elapsed_time(e1) * 1e3)
             med[name] = statistics.median(ts)
+            status = lk.device_status(stream)
+            if status:
+                raise RuntimeError(f"device status {status:#x} after the {phase} overhead run '{name}'")
         out[phase] = {"rot_us": med["rot"], "delta0_us": med["delta0"], "same_delta_us": med["same_delta"],
                       "overhead": med["rot"] / med["delta0"] - 1.0,
                       "boundary_share": (med["rot"] - med["same_delta"]) / med["delta0"]}
-    status = lk.device_status()
-    if status:
-        raise RuntimeError(f"device status {status:#x} after the overhead runs")
     out["method"] = ("same caches and inputs; rot = rotary kind of the workload, delta0 = kernels "
                      "without positional work, same_delta = rotary kernels with every Delta = 0; "
                      f"eager launches, L2 flushed before each, median of {reps} reps"

@@ -114,12 +114,27 @@ __device__ __forceinline__ uint64_t global_ns() {
 // LAZY_STATUS_TIMEOUT and leaves; the kernel never spins forever.
 constexpr uint64_t kWaitNs = 1500000000ull;  // 1.5 s
 
+// Time spent in one wait, from successive readings of the global timer.  Each reading adds
+// the step since the previous one clamped to [20 ns, 1 ms], so a jump of the timer (forwards
+// or backwards) cannot end a wait early, and a timer that stood still would still end it.
+struct WaitClock {
+  uint64_t last, spent;
+  __device__ __forceinline__ WaitClock() : last(global_ns()), spent(0) {}
+  __device__ __forceinline__ bool expired() {
+    const uint64_t now = global_ns();
+    const uint64_t d = now - last;  // a backwards jump wraps to a huge step, clamped below
+    last = now;
+    spent += d < 20ull ? 20ull : (d > 1000000ull ? 1000000ull : d);
+    return spent > kWaitNs;
+  }
+};
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  WaitClock clk;
   while (true) {
     if (mbar_test(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (clk.expired()) return false;
   }
 }
 

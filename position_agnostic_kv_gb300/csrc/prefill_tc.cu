@@ -198,13 +198,13 @@ __device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sy
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
   if (mbar_test(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  WaitClock clk;
   uint32_t n = 0;
   while (true) {
     if (mbar_test(bar, parity)) return true;
     if ((++n & 63u) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (clk.expired()) {
         *abort_flag = 1;
         set_status(status, LAZY_STATUS_TIMEOUT);
         return false;
@@ -763,14 +763,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       if (lane == 0) {
         for (int j = max(0, issued_k - kStages); j < issued_k; ++j) {
           const uint32_t bar = BAR(B_K_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
-          const uint64_t t0 = global_ns();
-          while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+          WaitClock clk;
+          while (!mbar_test(bar, par) && !clk.expired()) {
           }
         }
         for (int j = max(0, issued_v - kStages); j < issued_v; ++j) {
           const uint32_t bar = BAR(B_V_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
-          const uint64_t t0 = global_ns();
-          while (!mbar_test(bar, par) && global_ns() - t0 < kWaitNs) {
+          WaitClock clk;
+          while (!mbar_test(bar, par) && !clk.expired()) {
           }
         }
       }
@@ -899,8 +899,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         }
         // every MMA must be complete before TMEM is released (and before the epilogue reads O)
         mma_commit(BAR(B_FINAL));
-        const uint64_t t0 = global_ns();
-        while (!mbar_test(BAR(B_FINAL), 0) && global_ns() - t0 < kWaitNs) {
+        WaitClock clk;
+        while (!mbar_test(BAR(B_FINAL), 0) && !clk.expired()) {
         }
       }
       __syncwarp();
