@@ -194,10 +194,15 @@ def run_ours(args, dist):
     pb.fill_documents()
     torch.cuda.synchronize()
     n_dec = w.n_decode
-    pre = pb.upload_prefill() if pb.total_q else None
-    decs = [pb.upload_decode(t) for t in range(n_dec)]
-    out_p = torch.empty((max(pb.total_q, 1), w.Hq, w.D), dtype=torch.bfloat16, device=dev)
-    outs_d = [torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16, device=dev) for _ in range(n_dec)]
+    # Every step's inputs live in one device buffer and its outputs in another, so that the
+    # end-to-end run moves them with one host->device and one device->host copy per step.
+    in_blob, (pre, *decs) = pack_views([pb.upload_prefill() if pb.total_q else {}] +
+                                       [pb.upload_decode(t) for t in range(n_dec)], dev)
+    pre = pre or None
+    out_blob, outs = pack_views([{"o": torch.empty((max(pb.total_q, 1), w.Hq, w.D), dtype=torch.bfloat16)}] +
+                                [{"o": torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16)}
+                                 for _ in range(n_dec)], dev)
+    out_p, outs_d = outs[0]["o"], [o["o"] for o in outs[1:]]
     stream = torch.cuda.Stream(device=dev)
     use_graph = not args.no_graph
 
@@ -205,8 +210,12 @@ def run_ours(args, dist):
         return torch.cuda.Event(enable_timing=True, external=True) if use_graph else \
             torch.cuda.Event(enable_timing=True)
 
+    # Event pairs on the prefill and on every 8th decode launch: enough samples for the
+    # per-launch times, few enough event nodes to leave the step's own time unchanged.
+    ev_every = 8
+    ev_steps = list(range(0, n_dec, ev_every))
     ev_pre = (mk(), mk())
-    ev_dec = [(mk(), mk()) for _ in range(n_dec)]
+    ev_dec = {t: (mk(), mk()) for t in ev_steps}
     launches = 0
 
     def step():
@@ -223,10 +232,12 @@ def run_ours(args, dist):
         for t in range(n_dec):
             d = decs[t]
             lk.kv_write(d["k"], d["v"], d["slot"], d["lp"], pb.k_cache, pb.v_cache, pb.cfg, stream=stream)
-            ev_dec[t][0].record(stream)
+            if t in ev_dec:
+                ev_dec[t][0].record(stream)
             lk.attn_decode(d["q"], d["seq_len"], pb.q_start, pb.doc_blocks, pb.meta, pb.k_cache,
                            pb.v_cache, pb.cfg, outs_d[t], ws=pb.ws, stream=stream)
-            ev_dec[t][1].record(stream)
+            if t in ev_dec:
+                ev_dec[t][1].record(stream)
             launches += 1 + launches_of("decode", pb)
 
     # warm-up (also sets kernel attributes before any capture)
@@ -276,7 +287,7 @@ def run_ours(args, dist):
             try:
                 if pre is not None:
                     pre_ms.append(ev_pre[0].elapsed_time(ev_pre[1]))
-                dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
+                dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec.values())
             except RuntimeError as e:
                 print(f"[bench] in-graph event timing unavailable ({e})", file=sys.stderr)
                 inner_ok = False
@@ -286,15 +297,13 @@ def run_ours(args, dist):
     dist.barrier()
     clk = clocks.stop()
     if not inner_ok:  # per-launch times from eager launches of the same step, L2 flushed
-        eager = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(n_dec + 1)]
         for _ in range(min(args.steps, 10)):
             with torch.cuda.stream(stream):
                 flush.zero_()
                 step()
             stream.synchronize()
             pre_ms.append(ev_pre[0].elapsed_time(ev_pre[1]) if pre is not None else 0.0)
-            dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
+            dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec.values())
     status = lk.device_status()
     if status:
         raise RuntimeError(f"device status {status:#x} after the timed region")
@@ -311,7 +320,7 @@ def run_ours(args, dist):
         keys = keys0 + t + 1
         blocks = pb.doc_blocks_h.astype(np.int64) + (keys - 1 - pb.q_start_h) // 16 + 1
         dec_bytes.append(int(keys.sum()) * kv_row + 2 * w.B * w.Hq * w.D * 2 + int(blocks.sum()) * 8)
-    avg_dec_bytes = sum(dec_bytes) / max(n_dec, 1)
+    avg_dec_bytes = statistics.mean(dec_bytes[t] for t in ev_steps) if ev_steps else 0.0
     avg_dec_ms = statistics.mean(dec_ms) if dec_ms else 0.0
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
@@ -354,6 +363,7 @@ def run_ours(args, dist):
         "roofline": roofline,
         "decode": {"kernel": "lazy_attn_decode", "bytes_per_launch": avg_dec_bytes if dec_ms else None,
                    "avg_launch_us": avg_dec_ms * 1e3 if dec_ms else None, "gbs": achieved_gbs,
+                   "timed_launches": f"decode steps {ev_steps} of every timed step (CUDA events in the graph)",
                    "frac_hbm_peak": achieved_gbs / hbm_peak if achieved_gbs else None,
                    "launches_per_step": n_dec},
         "prefill": {"kernel": "lazy_attn_prefill", "flops_per_launch": pre_flops,
@@ -367,7 +377,7 @@ def run_ours(args, dist):
     if not args.no_overhead and pb.cfg.kind in (lk.POS_ROPE, lk.POS_YARN):
         res["rotation_overhead"] = rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush)
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, pb, pre, decs, out_p, outs_d, graph, run_step, stream, dist, tokens_per_step)
+        res["e2e"] = run_e2e(args, in_blob, out_blob, run_step, stream, dist, tokens_per_step)
     return res
 
 
@@ -434,38 +444,58 @@ def launches_of(phase: str, pb) -> int:
     return 1 + (1 if ws > 0 else 0)
 
 
-def run_e2e(args, pb, pre, decs, out_p, outs_d, graph, run_step, stream, dist, tokens_per_step):
-    """Same step, but every step's inputs start in pinned host memory and its outputs return
-    to pinned host memory: host->device copies, the step, device->host copies, all timed."""
+def pack_views(dicts, dev):
+    """One device buffer holding every tensor of `dicts` (each at a 256-byte aligned offset);
+    returns the buffer and the same dicts with each tensor replaced by its view in it."""
     import torch
-    host_in = []
-    for d in ([pre] if pre is not None else []) + decs:
-        host_in.append({k: v.cpu().pin_memory() for k, v in d.items()})
-    dev_in = ([pre] if pre is not None else []) + decs
-    outs = ([out_p[: pb.total_q]] if pre is not None else []) + outs_d
-    host_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = sum(t.numel() * t.element_size() for d in host_in for t in d.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    offs, total = [], 0
+    for d in dicts:
+        o = {}
+        for k, t in d.items():
+            o[k] = total
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        offs.append(o)
+    blob = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    views = []
+    for d, o in zip(dicts, offs):
+        v = {}
+        for k, t in d.items():
+            n = t.numel() * t.element_size()
+            v[k] = blob[o[k]:o[k] + n].view(t.dtype).view(t.shape)
+            v[k].copy_(t)
+        views.append(v)
+    return blob, views
+
+
+def run_e2e(args, in_blob, out_blob, run_step, stream, dist, tokens_per_step):
+    """Same step, but its inputs start in pinned host memory and its outputs return to pinned
+    host memory: one host->device copy of the step's packed inputs (query tokens and every
+    decode step's q, k, v, slots, positions, lengths), the step, one device->host copy of its
+    packed outputs (prefill and every decode step's attention output), all timed."""
+    import torch
+    host_in = in_blob.cpu().pin_memory()
+    host_out = torch.empty(out_blob.shape, dtype=out_blob.dtype).pin_memory()
+    h2d, d2h = in_blob.numel() * in_blob.element_size(), out_blob.numel() * out_blob.element_size()
     times = []
     n = max(3, min(args.steps, 50))
     for k in range(n + 2):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for hd, dd in zip(host_in, dev_in):
-                for key in dd:
-                    dd[key].copy_(hd[key], non_blocking=True)
+            in_blob.copy_(host_in, non_blocking=True)
             run_step()
-            for ho, o in zip(host_out, outs):
-                ho.copy_(o, non_blocking=True)
+            host_out.copy_(out_blob, non_blocking=True)
             e1.record(stream)
         stream.synchronize()
         if k >= 2:
             times.append(e0.elapsed_time(e1))
+    if not torch.equal(host_out.view(-1)[:1024], out_blob.view(-1)[:1024].cpu()):
+        raise RuntimeError("end-to-end outputs did not reach the host buffer")
     ms = dist.max(statistics.mean(times))
     return {"value": dist.world * tokens_per_step / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "steps": n, "api": "position_agnostic_kv_gb300 binding over liblazykv (C ABI), pinned host buffers"}
+            "steps": n, "api": "position_agnostic_kv_gb300 binding over liblazykv (C ABI); one packed "
+                               "pinned host buffer each way per step"}
 
 
 # ------------------------------------------------------------------ the oracle (CPU)

@@ -147,6 +147,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  Every kernel of the library is launched
+// so that it may become resident while the previous kernel of the stream drains; it calls
+// pdl_wait() before it reads or writes any global memory (that returns once the previous grid
+// has completed and its writes are visible), and pdl_trigger() once every one of its CTAs is
+// running, which lets the next kernel of the stream start its launch early.  Both are no-ops
+// when the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }
@@ -165,6 +174,23 @@ int check_device();                        // LAZY_EARCH unless CC 10.x
 int sm_count();                            // current device
 uint32_t* status_word();                   // device address of the status word (current device)
 int prepare_pos(const lazy_pos_cfg* cfg, int Hq, int D, float scale, PosParams* out);
+
+// Launch `kern` on `st` with programmatic stream serialisation (see pdl_wait above).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 #define LAZY_CUDA_TRY(expr)                                                              \
   do {                                                                                   \

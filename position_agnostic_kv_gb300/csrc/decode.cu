@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
   const int split = blockIdx.x, hg = blockIdx.y, r = blockIdx.z;
   const int h0 = hg * G;                       // first query head of this CTA
   const int kvh = h0 / (a.Hq / a.Hkv);         // its KV head (contiguous GQA grouping)
+  pdl_wait();
 
   // ---- the query row: request, absolute position m, visible blocks
   int b, m;
@@ -385,6 +386,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
     if (i + NST < n) issue(i + NST);
   }
 
+  pdl_trigger();  // every CTA of the grid is running once all have reached this point
+
   // ---- fold row groups, then the warps of the CTA
 #pragma unroll
   for (int off = LPR; off < 32; off <<= 1)
@@ -459,6 +462,8 @@ template <int D>
 __global__ void __launch_bounds__(D) merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                                   int S, int Hq, __nv_bfloat16* __restrict__ out,
                                                   float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   const size_t rh = blockIdx.x;  // row * Hq + head
   const int col = threadIdx.x;
   const float* ml = part_ml + rh * S * 2;
@@ -546,12 +551,10 @@ static int launch_t(const DecodeArgs& a, cudaStream_t st) {
     attr_set[dev & 63] = true;
   }
   dim3 grid(a.S, a.Hq / G, a.rows);
-  kern<<<grid, kDecWarps * 32, L::SMEM, st>>>(a);
-  LAZY_CUDA_TRY(cudaGetLastError());
-  if (a.S > 1) {
-    merge_kernel<D><<<(unsigned)a.rows * a.Hq, D, 0, st>>>(a.part_o, a.part_ml, a.S, a.Hq, a.out, a.lse);
-    LAZY_CUDA_TRY(cudaGetLastError());
-  }
+  LAZY_CUDA_TRY(launch_pdl(kern, grid, dim3(kDecWarps * 32), L::SMEM, st, a));
+  if (a.S > 1)
+    LAZY_CUDA_TRY(launch_pdl(merge_kernel<D>, dim3((unsigned)a.rows * a.Hq), dim3(D), 0, st,
+                             (const float*)a.part_o, (const float*)a.part_ml, a.S, a.Hq, a.out, a.lse));
   return LAZY_OK;
 }
 
@@ -595,10 +598,11 @@ int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_by
                             a.part_o, a.part_ml);
     if (rc || a.S == 1) return rc;
     if (D == 128)
-      merge_kernel<128><<<(unsigned)a.rows * a.Hq, 128, 0, st>>>(a.part_o, a.part_ml, a.S, a.Hq, a.out, a.lse);
+      LAZY_CUDA_TRY(launch_pdl(merge_kernel<128>, dim3((unsigned)a.rows * a.Hq), dim3(128), 0, st,
+                               (const float*)a.part_o, (const float*)a.part_ml, a.S, a.Hq, a.out, a.lse));
     else
-      merge_kernel<64><<<(unsigned)a.rows * a.Hq, 64, 0, st>>>(a.part_o, a.part_ml, a.S, a.Hq, a.out, a.lse);
-    LAZY_CUDA_TRY(cudaGetLastError());
+      LAZY_CUDA_TRY(launch_pdl(merge_kernel<64>, dim3((unsigned)a.rows * a.Hq), dim3(64), 0, st,
+                               (const float*)a.part_o, (const float*)a.part_ml, a.S, a.Hq, a.out, a.lse));
     return LAZY_OK;
   }
   a.group = decode_group(a.Hq, a.Hkv);

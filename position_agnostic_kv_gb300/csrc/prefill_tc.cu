@@ -258,6 +258,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   uint8_t* sm = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = int(blockIdx.x) % a.S, mp = int(blockIdx.x) / a.S, g = blockIdx.y, b = blockIdx.z;
+  pdl_wait();
   const int G = a.Hq / a.Hkv;
   const int tpt = kM / G;  // tokens per Q tile
   const int qs = a.q_start[b];
@@ -907,6 +908,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   }
 
+  pdl_trigger();  // every CTA of the grid is running once all have reached this point
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -980,8 +982,7 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
   const int G = a.Hq / a.Hkv;
   const int rows_tok = tc::kQT * (tc::kM / G);  // tokens per CTA
   dim3 grid(unsigned((max_q + rows_tok - 1) / rows_tok) * unsigned(a.S), a.Hkv, a.B);
-  kern<<<grid, tc::kThreads, L::SMEM, st>>>(mk, mv, a);
-  LAZY_CUDA_TRY(cudaGetLastError());
+  LAZY_CUDA_TRY(launch_pdl(kern, grid, dim3(tc::kThreads), L::SMEM, st, mk, mv, a));
   return LAZY_OK;
 }
 

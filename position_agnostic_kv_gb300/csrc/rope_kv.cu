@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) kv_write_kernel(const uint4* __restrict__
                                                        int num_pages, PosParams pos, uint32_t* status) {
   constexpr int TPR = D / 16;       // threads per (token, head)
   constexpr int CH = D / 8;         // 16-byte chunks per row
+  pdl_wait();
+  pdl_trigger();  // one small wave: every CTA is running
   const long long gid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long row = gid / TPR;  // (token, head)
   const int part = int(gid % TPR);
@@ -163,13 +165,9 @@ extern "C" int lazy_kv_write(const void* k, const void* v, const int32_t* slot, 
   const uint4* v4 = static_cast<const uint4*>(v);
   uint4* kc = static_cast<uint4*>(k_cache);
   uint4* vc = static_cast<uint4*>(v_cache);
-  if (D == 128) {
-    if (rotate) kv_write_kernel<128, true><<<blocks, threads, 0, st>>>(k4, v4, slot, local_pos, T, Hkv, kc, vc, num_pages, pos, status);
-    else kv_write_kernel<128, false><<<blocks, threads, 0, st>>>(k4, v4, slot, local_pos, T, Hkv, kc, vc, num_pages, pos, status);
-  } else {
-    if (rotate) kv_write_kernel<64, true><<<blocks, threads, 0, st>>>(k4, v4, slot, local_pos, T, Hkv, kc, vc, num_pages, pos, status);
-    else kv_write_kernel<64, false><<<blocks, threads, 0, st>>>(k4, v4, slot, local_pos, T, Hkv, kc, vc, num_pages, pos, status);
-  }
-  LAZY_CUDA_TRY(cudaGetLastError());
+  auto kern = D == 128 ? (rotate ? kv_write_kernel<128, true> : kv_write_kernel<128, false>)
+                       : (rotate ? kv_write_kernel<64, true> : kv_write_kernel<64, false>);
+  LAZY_CUDA_TRY(launch_pdl(kern, dim3(blocks), dim3(threads), 0, st, k4, v4, slot, local_pos, T, Hkv, kc, vc,
+                           num_pages, pos, status));
   return LAZY_OK;
 }
