@@ -435,7 +435,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             wait_bar(BAR(B_S_FULL + buf), uint32_t(nq == 2 ? (j & 1) : ((j >> 1) & 1)), abort_flag, a.status);
         if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
         tc_fence_after();
-        const bool fast = (POS != kAlibi) && flags[slot * 2];
+        const bool fast = flags[slot * 2] != 0;  // every key of the tile is visible to every row
         // the whole S row in registers: four loads, one wait
         uint32_t v[kN];
         tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
@@ -443,7 +443,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
         tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
         tmem_wait_ld();
-        if (!fast) {  // key p = start + t of a page is visible iff t < rows and p <= m
+        if (POS == kAlibi && fast) {  // bias only: -slope (m - p), p = start + t
+#pragma unroll
+          for (int pp = 0; pp < kPagesPerTile; ++pp) {
+            const float base = slope * float(pstart[slot * kPagesPerTile + pp] - m_row);
+#pragma unroll
+            for (int t = 0; t < kPage; ++t)
+              v[pp * kPage + t] = __float_as_uint(__uint_as_float(v[pp * kPage + t]) + fmaf(slope, float(t), base));
+          }
+        } else if (!fast) {  // key p = start + t of a page is visible iff t < rows and p <= m
 #pragma unroll
           for (int pp = 0; pp < kPagesPerTile; ++pp) {
             const int st = pstart[slot * kPagesPerTile + pp];
@@ -676,8 +684,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       // V stage once both its PV are done, and no K load waits behind an earlier tile's PV.
       const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
       int* pgid = reinterpret_cast<int*>(sm + L::PGID_OFF);
+      // With ALiBi the bias grows towards the query, so the newest keys hold each row's maximum:
+      // visiting the tiles newest first fixes the running max at once and the O rescale of the
+      // lazy softmax (only when a max grows by more than 8) almost never runs.  Softmax is
+      // indifferent to key order, and every per-tile fact travels with the tile's slot.
+      auto tile_of = [&](int j) { return POS == kAlibi ? t0 + ntiles - 1 - j : t0 + j; };
       auto fetch = [&](int j) -> uint64_t {  // lane < 8: block word of page slot `lane` of tile j
-        const int jb = (t0 + j) * kPagesPerTile + lane;
+        const int jb = tile_of(j) * kPagesPerTile + lane;
         return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
       };
       uint64_t w_next = fetch(0);
@@ -688,7 +701,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const uint64_t w = w_next;
         w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
         int rows = 0, start = 0, page = 0, delta = 0;
-        const int jb = (t0 + j) * kPagesPerTile + lane;
+        const int jb = tile_of(j) * kPagesPerTile + lane;
         if (lane < kPagesPerTile && jb < nb) {
           page = int(word_page(w));
           delta = int(word_delta(w));
