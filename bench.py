@@ -178,6 +178,13 @@ def profiled_traffic(kernel_src: str, name: str):
     return float(m_t.group(1))
 
 
+def job_throughput(dist, tokens_per_step: int, step_ms: list) -> tuple:
+    """Whole-job throughput of a replicas-only run: every rank processes `tokens_per_step` per
+    step, and the job's step time is the slowest rank's mean (max over ranks)."""
+    mean_ms = dist.max(sum(step_ms) / len(step_ms))
+    return dist.world * tokens_per_step / (mean_ms / 1e3), mean_ms
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist):
     import numpy as np
@@ -309,8 +316,7 @@ def run_ours(args, dist):
         raise RuntimeError(f"device status {status:#x} after the timed region")
 
     tokens_per_step = pb.total_q + w.B * n_dec
-    mean_ms = dist.max(sum(step_ms) / len(step_ms))
-    value = dist.world * tokens_per_step / (mean_ms / 1e3)
+    value, mean_ms = job_throughput(dist, tokens_per_step, step_ms)
 
     # algorithmic units (sizes only): decode bytes per launch, prefill flops per launch
     keys0 = pb.seq_len0_h.astype(np.int64)
