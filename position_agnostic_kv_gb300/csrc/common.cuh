@@ -58,6 +58,16 @@ __device__ __forceinline__ void turn_sincos(uint32_t p, unsigned long long turns
   sincospif(half_turns, &s, &c);                                     // sin/cos(pi * x)
 }
 
+// The same angle through the SFU's sine and cosine (__sincosf).  The exact turn count leaves
+// an argument in [-pi, pi), where the hardware approximation is good to about 1e-6 absolute:
+// used where the rotated values stay in fp32 (a query rotated at a document boundary), not
+// where they are rounded into a stored or tensor-core operand.
+__device__ __forceinline__ void turn_sincos_fast(uint32_t p, unsigned long long turns, float& s, float& c) {
+  const unsigned long long frac = (unsigned long long)p * turns;
+  const int hi = int(uint32_t(frac >> 32));
+  __sincosf(float(hi) * 1.4629180792671596e-9f, &s, &c);  // * pi * 2^-31 -> [-pi, pi)
+}
+
 // ------------------------------------------------------------------------------------------
 // bf16 <-> fp32
 // ------------------------------------------------------------------------------------------

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
               cs[e] = a.pos.table[(size_t)dp * rd + fi];
               sn[e] = a.pos.table[(size_t)dp * rd + hr + fi];
             } else {
-              turn_sincos(dp, a.pos.turns[fi], sn[e], cs[e]);
+              turn_sincos_fast(dp, a.pos.turns[fi], sn[e], cs[e]);
             }
           }
 #pragma unroll
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
               cs[e] = a.pos.table[(size_t)dp * D + i0 + e];
               sn[e] = a.pos.table[(size_t)dp * D + D / 2 + i0 + e];
             } else {
-              turn_sincos(dp, a.pos.turns[i0 + e], sn[e], cs[e]);
+              turn_sincos_fast(dp, a.pos.turns[i0 + e], sn[e], cs[e]);
             }
           }
 #pragma unroll
