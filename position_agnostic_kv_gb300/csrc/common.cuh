@@ -59,9 +59,10 @@ __device__ __forceinline__ void turn_sincos(uint32_t p, unsigned long long turns
 }
 
 // The same angle through the SFU's sine and cosine (__sincosf).  The exact turn count leaves
-// an argument in [-pi, pi), where the hardware approximation is good to about 1e-6 absolute:
-// used where the rotated values stay in fp32 (a query rotated at a document boundary), not
-// where they are rounded into a stored or tensor-core operand.
+// an argument in [-pi, pi), where the hardware approximation is good to about 1e-6 absolute,
+// far below the rounding the rotated value gets next in the attention kernels (an f16 operand
+// of the tensor cores, or an fp32 query); the stored keys (kv_write) and the cos/sin table keep
+// the correctly rounded sincospif.
 __device__ __forceinline__ void turn_sincos_fast(uint32_t p, unsigned long long turns, float& s, float& c) {
   const unsigned long long frac = (unsigned long long)p * turns;
   const int hi = int(uint32_t(frac >> 32));

@@ -374,7 +374,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             co = a.pos.table[(size_t)m * rd + i];
             sn = a.pos.table[(size_t)m * rd + hr + i];
           } else {
-            turn_sincos(m, turns[i], sn, co);
+            turn_sincos_fast(m, turns[i], sn, co);
           }
         };
         if (!a.pos.interleaved) {
@@ -576,8 +576,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           const int dl = pinfo[slot * kPagesPerTile + pp].x;
           if (prun[slot * kPagesPerTile + pp] == pp) {
             float s0, c0, s1, c1;
-            turn_sincos(uint32_t(dl), turns[2 * q], s0, c0);
-            turn_sincos(uint32_t(dl), turns[2 * q + 1], s1, c1);
+            turn_sincos_fast(uint32_t(dl), turns[2 * q], s0, c0);
+            turn_sincos_fast(uint32_t(dl), turns[2 * q + 1], s1, c1);
             cs4[idx] = make_float4(c0, c1, s0, s1);
           }
         }
