@@ -98,8 +98,9 @@ struct Layout {
   static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, clean}
   static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] physical pages
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
-  static constexpr int CS_OFF = TURNS_OFF + (D / 2) * 8;                // float2 [8][D/2]
-  static constexpr int BAR_OFF = CS_OFF + kPagesPerTile * (D / 2) * 8;
+  static constexpr int CS_OFF = TURNS_OFF + (D / 2) * 8;                // float2 [2][8][D/2]
+  static constexpr int CS_BUF = kPagesPerTile * (D / 4);                 // float4 per buffer
+  static constexpr int BAR_OFF = CS_OFF + 2 * kPagesPerTile * (D / 2) * 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;                   // tmem slot, abort flag
   static constexpr int SMEM = MISC_OFF + 16 + 1024;                     // + alignment slack
 };
@@ -578,12 +579,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             float s0, c0, s1, c1;
             turn_sincos_fast(uint32_t(dl), turns[2 * q], s0, c0);
             turn_sincos_fast(uint32_t(dl), turns[2 * q + 1], s1, c1);
-            cs4[idx] = make_float4(c0, c1, s0, s1);
+            cs4[(j & 1) * L::CS_BUF + idx] = make_float4(c0, c1, s0, s1);
           }
         }
         named_sync(1, 128);
         if (ok && t < pi.y) {
-          const float4* c4 = cs4 + run_start * (D / 4);
+          const float4* c4 = cs4 + (j & 1) * L::CS_BUF + run_start * (D / 4);
           const int rd = a.pos.rotary_dim;
           if (rd == D && !a.pos.interleaved) {  // full half-split rotation (the common case)
 #pragma unroll
@@ -656,7 +657,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           }
         }
         fence_async_smem();
-        named_sync(1, 128);  // cos/sin table reused next tile
       }
       mbar_arrive(BAR(B_K_READY + s));
       // V: rows holding no key are cleared so no stale bits reach the tensor core.  Waiting for
