@@ -124,17 +124,18 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
   const uint32_t bar0 = smem_u32(smem + L::BAR_OFF + warp * NST * 8);
   const uint32_t stage0 = smem_u32(smem + warp * NST * L::STAGE_BYTES);
 
+  // ---- block words of this warp's run, 32 at a time (coalesced), next chunk prefetched; issued
+  // before the query loads so that the two latencies overlap
+  const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks + wb;
+  uint64_t mcur = lane < n ? ldg_u64(mrow + lane) : 0;
+  uint64_t mnxt = 32 + lane < n ? ldg_u64(mrow + 32 + lane) : 0;
+  int mbase = 0;
+
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = __bfloat162float(qrow[h0 * D + i]);
   if (lane == 0)
     for (int s = 0; s < NST; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
   __syncthreads();
-
-  // ---- block words of this warp's run, 32 at a time (coalesced), next chunk prefetched
-  const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks + wb;
-  uint64_t mcur = lane < n ? ldg_u64(mrow + lane) : 0;
-  uint64_t mnxt = 32 + lane < n ? ldg_u64(mrow + 32 + lane) : 0;
-  int mbase = 0;
 
   const size_t head_stride = (size_t)kPage * D;  // elements per (page, head)
   auto issue = [&](int i) {
