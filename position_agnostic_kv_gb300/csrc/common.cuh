@@ -69,6 +69,13 @@ __device__ __forceinline__ void turn_sincos_fast(uint32_t p, unsigned long long 
   __sincosf(float(hi) * 1.4629180792671596e-9f, &s, &c);  // * pi * 2^-31 -> [-pi, pi)
 }
 
+// 2^x on the SFU (ex2.approx, flush-to-zero; 2^-inf = 0), for softmax weights.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------------------------------
 // bf16 <-> fp32
 // ------------------------------------------------------------------------------------------

@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
     for (int e = 0; e < E; ++e) {
       const int rr = (base_idx + e) % RPL;
       const int row = rr * RPI + rg;
-      const float p = exp2f(s2[e] - mr);
+      const float p = ex2_approx(s2[e] - mr);
       if (unique) {
         l_lane += p;
         pbuf[row * G + h_lane] = p;
