@@ -562,6 +562,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     const int rt = threadIdx.x - kRotWarp0 * 32;
     const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
     bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
+    // A tile whose pages are one run of the same Delta as the previous tile's single run (the
+    // middle of a long document) reuses that tile's cos/sin buffer; otherwise the rows go to the
+    // other buffer, which no thread still reads once all passed the previous tile's barrier.
+    int cs_buf = 1, cs_delta = -1;  // buffer and Delta of the last single-run tile (-1: none)
     for (int j = 0; j < ntiles; ++j) {
       const int s = j % kStages, slot = j % kSlots;
       const uint32_t par = uint32_t((j / kStages) & 1);
@@ -572,19 +576,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         // cos/sin rows only for pages that start a new document offset: page pp uses the row of
         // the first page of its run of equal Delta (consecutive pages of a document share it)
         const int run_start = ok ? prun[slot * kPagesPerTile + ps] : 0;
-        for (int idx = rt; ok && idx < kPagesPerTile * (D / 4); idx += 128) {
+        const int d0 = ok ? pinfo[slot * kPagesPerTile].x : -1;
+        const bool single = ok && prun[slot * kPagesPerTile + kPagesPerTile - 1] == 0;  // same for all
+        const bool reuse = single && d0 == cs_delta;
+        if (!reuse) cs_buf ^= 1;
+        cs_delta = single ? d0 : -1;
+        for (int idx = rt; ok && !reuse && idx < kPagesPerTile * (D / 4); idx += 128) {
           const int pp = idx / (D / 4), q = idx % (D / 4);
           const int dl = pinfo[slot * kPagesPerTile + pp].x;
           if (prun[slot * kPagesPerTile + pp] == pp) {
             float s0, c0, s1, c1;
             turn_sincos_fast(uint32_t(dl), turns[2 * q], s0, c0);
             turn_sincos_fast(uint32_t(dl), turns[2 * q + 1], s1, c1);
-            cs4[(j & 1) * L::CS_BUF + idx] = make_float4(c0, c1, s0, s1);
+            cs4[cs_buf * L::CS_BUF + idx] = make_float4(c0, c1, s0, s1);
           }
         }
         named_sync(1, 128);
         if (ok && t < pi.y) {
-          const float4* c4 = cs4 + (j & 1) * L::CS_BUF + run_start * (D / 4);
+          const float4* c4 = cs4 + cs_buf * L::CS_BUF + run_start * (D / 4);
           const int rd = a.pos.rotary_dim;
           if (rd == D && !a.pos.interleaved) {  // full half-split rotation (the common case)
 #pragma unroll
