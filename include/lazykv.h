@@ -20,6 +20,10 @@
  *     head is 16 * D * 2 bytes, contiguous.  A cache slot is page * 16 + row.
  *   - Every GPU entry point is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), performs no synchronisation and returns after the launch.
+ *   - Kernels are launched with programmatic dependent launch: one may become resident while
+ *     the previous kernel of the stream drains, and it reads or writes no global memory until
+ *     that kernel has completed (griddepcontrol.wait), so stream order is kept exactly as for
+ *     a plain launch, including inside CUDA graph capture.
  *   - Return codes: LAZY_OK, or a negative code with a message for lazy_last_error().
  *     Argument errors are detected on the host before anything is launched.  Errors found
  *     by a kernel (an out-of-range page or slot, a wait that ran out) set bits of the device
