@@ -95,9 +95,78 @@ __global__ void __launch_bounds__(64, 1) stream(const __grid_constant__ CUtensor
   if (MC == 2) cluster_sync(); else __syncthreads();
 }
 
+// One CTA per SM with P producer warps, each streaming its own NST-stage ring (own barriers)
+// and one consumer lane per ring: do several independent rings in one CTA reach the rate of
+// several CTAs?
+template <int NST, int P>
+__global__ void __launch_bounds__(64 * P, 1) stream_multi(const __grid_constant__ CUtensorMap map, const int* page_ids,
+                                                          int n_pages_total, int tiles, int* fail) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t s0 = (uint32_t(__cvta_generic_to_shared(smem)) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ring = warp >> 1;                       // warps 2r (producer), 2r+1 (consumer)
+  const uint32_t rbase = s0 + ring * NST * STAGE;
+  const uint32_t bars = s0 + P * NST * STAGE + ring * 2 * NST * 8;
+  if (lane == 0 && (warp & 1) == 0) {
+    for (int s = 0; s < NST; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8 * s));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8 * (NST + s)));
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int unit = blockIdx.x * P + ring;
+  if ((warp & 1) == 0) {
+    for (int j = 0; j < tiles; ++j) {
+      const int s = j % NST;
+      if (j >= NST && !wait_par(bars + 8 * (NST + s), ((j / NST) - 1) & 1)) { if (lane == 0) atomicAdd(fail, 1); break; }
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bars + 8 * s), "r"(STAGE) : "memory");
+      __syncwarp();
+      if (lane < PAGES) {
+        const int pg = page_ids[(unit * 7919 + j * PAGES + lane) % n_pages_total];
+        const uint32_t dst = rbase + s * STAGE + lane * PAGE_BYTES;
+        for (int cb = 0; cb < 2; ++cb)
+          asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                       ::"r"(dst + cb * 2048), "l"(reinterpret_cast<uint64_t>(&map)), "r"(cb * 64), "r"(pg * 16), "r"(bars + 8 * s) : "memory");
+      }
+      __syncwarp();
+    }
+  } else if (lane == 0) {
+    for (int j = 0; j < tiles; ++j) {
+      const int s = j % NST;
+      if (!wait_par(bars + 8 * s, (j / NST) & 1)) { atomicAdd(fail, 1); break; }
+      asm volatile("mbarrier.arrive.release.cluster.shared::cta.b64 _, [%0];" ::"r"(bars + 8 * (NST + s)) : "memory");
+    }
+  }
+  __syncthreads();
+}
+
+template <int NST, int P>
+int run_multi(const CUtensorMap& map, const int* ids, int n_pages, int grid, int tiles, int* fail) {
+  auto kern = stream_multi<NST, P>;
+  const int smem = P * NST * STAGE + P * 2 * NST * 8 + 1024;
+  CK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  float best = 1e30f;
+  for (int rep = 0; rep < 3; ++rep) {
+    cudaEvent_t a, b; cudaEventCreate(&a); cudaEventCreate(&b);
+    cudaEventRecord(a);
+    kern<<<grid, 64 * P, smem>>>(map, ids, n_pages, tiles, fail);
+    cudaEventRecord(b); CK(cudaEventSynchronize(b)); CK(cudaGetLastError());
+    float ms; cudaEventElapsedTime(&ms, a, b); if (ms < best) best = ms;
+  }
+  int f; CK(cudaMemcpy(&f, fail, 4, cudaMemcpyDeviceToHost));
+  const double arrived = (double)grid * P * tiles * STAGE;
+  printf("tma-%d-rings/CTA NST %d grid %3d: %8.1f us  arriving per SM %6.1f GB/s  fetched total %7.1f GB/s  fail %d\n", P, NST,
+         grid, best * 1e3, arrived / best / 1e6 / grid, arrived / best / 1e6, f);
+  return 0;
+}
+
 typedef CUresult (*EncFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
                           const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                           CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static int g_sms = 0;  // SM count: "per SM" divides by min(grid, SMs) (grids above it put 2 CTAs on an SM)
 
 template <int NST, int MC, bool BULK = false>
 int run(const CUtensorMap& map, const uint8_t* base, const int* ids, int n_pages, int grid, int tiles, int* fail,
@@ -121,13 +190,15 @@ int run(const CUtensorMap& map, const uint8_t* base, const int* ids, int n_pages
   }
   int f; CK(cudaMemcpy(&f, fail, 4, cudaMemcpyDeviceToHost));
   const double arrived = (double)grid * tiles * STAGE;  // bytes landing in shared memory, all CTAs
+  const int sms_used = grid < g_sms ? grid : g_sms;
   printf("%-14s NST %d grid %3d: %8.1f us  arriving per SM %6.1f GB/s  fetched total %7.1f GB/s  fail %d\n", name, NST, grid,
-         best * 1e3, arrived / best / 1e6 / grid, arrived / MC / best / 1e6, f);
+         best * 1e3, arrived / best / 1e6 / sms_used, arrived / MC / best / 1e6, f);
   return 0;
 }
 
 int main() {
   int sms = 0; CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0));
+  g_sms = sms;
   const int n_pages = 1 << 18;
   uint8_t* buf; CK(cudaMalloc(&buf, (size_t)n_pages * PAGE_BYTES));
   CK(cudaMemset(buf, 1, (size_t)n_pages * PAGE_BYTES));
@@ -154,6 +225,16 @@ int main() {
     if (run<2, 2>(map, buf, d_ids, n_pages, grid, tiles, fail, "tma-multicast")) return 1;
     if (run<4, 2>(map, buf, d_ids, n_pages, grid, tiles, fail, "tma-multicast")) return 1;
     if (run<4, 1, true>(map, buf, d_ids, n_pages, grid, tiles, fail, "bulk-4KB")) return 1;
+  }
+  // one CTA per SM with two or three independent rings (producer warp + barriers each)
+  if (run_multi<3, 2>(map, d_ids, n_pages, sms, tiles, fail)) return 1;
+  if (run_multi<2, 3>(map, d_ids, n_pages, sms, tiles, fail)) return 1;
+  // two CTAs per SM (each with half the ring): does the rate per SM grow with issuing CTAs?
+  {
+    const int grid = 2 * sms;
+    if (run<2, 1>(map, buf, d_ids, n_pages, grid, tiles, fail, "tma-2cta/SM")) return 1;
+    if (run<3, 1>(map, buf, d_ids, n_pages, grid, tiles, fail, "tma-2cta/SM")) return 1;
+    if (run<3, 1, true>(map, buf, d_ids, n_pages, grid, tiles, fail, "bulk-2cta/SM")) return 1;
   }
   return 0;
 }
