@@ -16,10 +16,12 @@
 //    every lane forms G x (rows per lane) partial dot products with packed fp32x2 FMAs, then a
 //    transposed butterfly over the row's lanes leaves each lane with complete scores.
 //  * q_eff = R_{m - Delta} q_raw, pre-multiplied by scale * log2(e), is recomputed in registers
-//    when Delta changes (cos/sin from the table or from exact fixed-point turns).
+//    when Delta changes (cos/sin from the table, or from exact fixed-point turns followed by the
+//    SFU's sine/cosine).
 //  * Online softmax in base 2 with a lazy max: the running max moves only when a score beats
 //    it by more than 8 (a warp vote), so the common page needs no max reduction.
-//  * Each CTA merges its warps; splits are merged by lse in a second small kernel.
+//  * Each CTA merges its warps; splits are merged by lse in a second small kernel, launched
+//    with programmatic dependent launch so its launch overlaps this kernel's tail.
 //  * "Rows" mode runs the same kernel with one query row per prefill token (causal limit
 //    m = q_start + i): the simple correct prefill used for shapes without a tensor-core path.
 #include <cfloat>

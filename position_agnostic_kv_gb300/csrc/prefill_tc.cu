@@ -15,8 +15,9 @@
 //              online softmax in base 2 (the running max moves, and O is rescaled in TMEM, only
 //              when a row's max grows by more than 8), P written back to TMEM over S as bf16.
 //   warps 8-11 K rotation: each staged K tile's page rows rotated by their page's Delta in
-//              place in shared memory (cos/sin only per distinct Delta); V rows that hold no key
-//              are zeroed so no stale bits reach the tensor core.
+//              place in shared memory (cos/sin rows only per distinct Delta, double-buffered,
+//              reused while consecutive tiles stay inside one document); V rows that hold no
+//              key are zeroed so no stale bits reach the tensor core.
 //   warp 12    producer: unpacks the 64-bit block words of a tile's 8 pages (prefetched one tile
 //              ahead) and issues TMA loads (box 16 rows x 64 columns, 128-byte swizzle) into
 //              2-stage K and V rings.
@@ -32,6 +33,7 @@
 // GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
 // Decode mode serves wide head groups (MQA): the G heads of one new token fill the rows, the
 // key range is split over several CTAs and their partials are merged by log-sum-exp.
+// With ALiBi the tiles are visited newest first (the running max is fixed by the first tile).
 // Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
 #include <cfloat>
 #include <climits>
