@@ -1,0 +1,338 @@
+"""Discrete-event model of the tensor-core attention kernel's mbarrier protocol (test
+infrastructure, host only).
+
+The roles of prefill_tc_kernel (K/V producer, K rotation and V cleaning, softmax of each Q tile,
+MMA issuer) are generators that yield ('wait', barrier, phase) or ('step',), in the same order
+of waits, arrivals and commits as the kernel, for both schedules (two live Q tiles, and one live
+Q tile whose scores alternate between the two S buffers).  Asynchronous engines: TMA copies land
+in any order; the tensor pipe runs MMAs in issue order and a commit arrives once every earlier
+MMA is done.  A random scheduler interleaves everything.  Checked: no deadlock; no parity
+aliasing (a barrier completing two phases past a waiter's, which try_wait.parity cannot tell
+apart); no metadata slot overwritten while a reader still needs it; no K/V stage refilled
+before all its consumers are done; S/P tensor-memory buffers written in a safe order.
+"""
+import random
+
+
+class ProtocolError(Exception):
+    pass
+
+
+class Bar:
+    def __init__(self, name, need):
+        self.name, self.need = name, need
+        self.arr, self.tx, self.k = 0, 0, 0
+        self.waiters = []  # (actor, phase)
+
+    def _check(self, sim):
+        if self.arr == self.need and self.tx == 0:
+            self.arr = 0
+            self.k += 1
+            for a, e in self.waiters:
+                if e < self.k - 1:
+                    raise ProtocolError(f"aliasing on {self.name}: waiter {a} wants phase {e}, barrier at {self.k}")
+
+    def arrive(self, sim, expect_tx=0):
+        self.arr += 1
+        self.tx += expect_tx
+        if self.arr > self.need:
+            raise ProtocolError(f"{self.name}: too many arrivals")
+        self._check(sim)
+
+    def complete_tx(self, sim, b):
+        self.tx -= b
+        self._check(sim)
+
+
+class Sim:
+    def __init__(self, ntiles, nq, clean, seed=0, slots=4):
+        self.rng = random.Random(seed)
+        self.n, self.nq, self.clean_of = ntiles, nq, clean
+        self.slots = slots
+        B = lambda name, need: Bar(name, need)
+        self.K_FULL = [B(f"K_FULL{s}", 1) for s in range(2)]
+        self.K_READY = [B(f"K_READY{s}", 1) for s in range(2)]
+        self.K_FREE = [B(f"K_FREE{s}", 1) for s in range(2)]
+        self.V_FULL = [B(f"V_FULL{s}", 1) for s in range(2)]
+        self.V_READY = [B(f"V_READY{s}", 1) for s in range(2)]
+        self.V_FREE = [B(f"V_FREE{s}", 1) for s in range(2)]
+        self.S_FULL = [B(f"S_FULL{i}", 1) for i in range(2)]
+        self.P_FULL = [B(f"P_FULL{i}", 1) for i in range(2)]
+        self.PV_DONE = B("PV_DONE", 1)
+        self.Q_READY = B("Q_READY", 2)
+        self.FINAL = B("FINAL", 1)
+        # state for hazard checks
+        self.slot_tile = [None] * self.slots
+        self.kstage = [None, None]      # tile whose K is in the stage (landed)
+        self.vstage = [None, None]
+        self.kstage_users = [set(), set()]  # outstanding consumers of the stage's tile
+        self.vstage_users = [set(), set()]
+        self.tma = []      # pending copies: (kind, stage, tile, bar, tx)
+        self.pipe = []     # tensor pipe FIFO: ('mma', fn) or ('commit', bar)
+        self.s_buf = {}    # S/P buffer -> ('S', tile) / ('P', tile) for hazard checks
+        self.done_qk = set()
+        self.done_pv = set()
+        self.p_written = set()
+
+    # ------------------------------------------------------------------ hazards
+    def read_slot(self, j, who):
+        s = j % self.slots
+        if self.slot_tile[s] != j:
+            raise ProtocolError(f"{who} reads slot {s} for tile {j}, holds {self.slot_tile[s]}")
+
+    def publish(self, j):
+        s = j % self.slots
+        self.slot_tile[s] = j
+
+    # ------------------------------------------------------------------ engines
+    def issue_tma(self, kind, j, bar, tx=1):
+        st = j % 2
+        users = self.kstage_users[st] if kind == "K" else self.vstage_users[st]
+        if users:
+            raise ProtocolError(f"{kind}({j}) issued into stage {st} while {sorted(users)} still use it")
+        self.tma.append((kind, st, j, bar))
+
+    def step_tma(self):
+        if not self.tma:
+            return False
+        i = self.rng.randrange(len(self.tma))
+        kind, st, j, bar = self.tma.pop(i)
+        if kind == "K":
+            self.kstage[st] = j
+            self.kstage_users[st] = {"rot", "qk0"} | ({"qk1"} if self.nq == 2 else set())
+        else:
+            self.vstage[st] = j
+            self.vstage_users[st] = {"pv0"} | ({"pv1"} if self.nq == 2 else set()) | (
+                {"clean"} if self.clean_of(j) else set())
+        bar.complete_tx(self, 1)
+        return True
+
+    def step_pipe(self):
+        if not self.pipe:
+            return False
+        op = self.pipe.pop(0)
+        if op[0] == "commit":
+            op[1].arrive(self)
+        else:
+            op[1]()
+        return True
+
+    # ------------------------------------------------------------------ MMAs
+    def qk(self, i, j, buf):
+        def run():
+            st = j % 2
+            if self.kstage[st] != j or "rot" in self.kstage_users[st]:
+                raise ProtocolError(f"QK{i}({j}) reads K stage {st} holding {self.kstage[st]} (rotated: {'rot' not in self.kstage_users[st]})")
+            prev = self.s_buf.get(buf)
+            if prev is not None and prev[0] == "P" and (i, prev[1]) not in self.done_pv:
+                raise ProtocolError(f"QK{i}({j}) overwrites P({prev[1]}) in S{buf} before its PV")
+            if prev is not None and prev[0] == "S":
+                raise ProtocolError(f"QK{i}({j}) overwrites S({prev[1]}) in S{buf} before the softmax read it")
+            self.s_buf[buf] = ("S", j)
+            self.kstage_users[st].discard(f"qk{i}")
+            self.done_qk.add((i, j))
+        self.pipe.append(("mma", run))
+
+    def pv(self, i, j, buf):
+        def run():
+            st = j % 2
+            if self.vstage[st] != j or "clean" in self.vstage_users[st]:
+                raise ProtocolError(f"PV{i}({j}) reads V stage {st} holding {self.vstage[st]}")
+            if self.s_buf.get(buf) != ("P", j):
+                raise ProtocolError(f"PV{i}({j}) reads S{buf} holding {self.s_buf.get(buf)}")
+            self.vstage_users[st].discard(f"pv{i}")
+            self.done_pv.add((i, j))
+        self.pipe.append(("mma", run))
+
+    def commit(self, bar):
+        self.pipe.append(("commit", bar))
+
+    # ------------------------------------------------------------------ actors
+    def producer(self):
+        n = self.n
+
+        def issue_k(j):  # wait for the stage, publish the tile's metadata, load K
+            s = j % 2
+            if j >= 2:
+                yield ("wait", self.K_FREE[s], j // 2 - 1)
+            self.publish(j)
+            self.K_FULL[s].arrive(self, expect_tx=1)
+            self.issue_tma("K", j, self.K_FULL[s])
+            yield ("step",)
+
+        def issue_v(j):
+            s = j % 2
+            if j >= 2:
+                yield ("wait", self.V_FREE[s], j // 2 - 1)
+            self.read_slot(j, "issue_v")
+            self.V_FULL[s].arrive(self, expect_tx=1)
+            self.issue_tma("V", j, self.V_FULL[s])
+            yield ("step",)
+
+        # issue order K0, K1, V0, K2, V1, ...
+        yield from issue_k(0)
+        for j in range(n):
+            if j + 1 < n:
+                yield from issue_k(j + 1)
+            yield from issue_v(j)
+
+    def rotation(self):
+        for j in range(self.n):
+            s = j % 2
+            yield ("wait", self.K_FULL[s], j // 2)
+            self.read_slot(j, "rotation")
+            yield ("step",)  # rotate in place
+            if self.kstage[s] != j:
+                raise ProtocolError(f"rotation of K({j}) finds stage holding {self.kstage[s]}")
+            self.kstage_users[s].discard("rot")
+            self.K_READY[s].arrive(self)
+            self.read_slot(j, "rotation-clean")
+            if self.clean_of(j):
+                yield ("wait", self.V_FULL[s], j // 2)
+                if self.vstage[s] != j:
+                    raise ProtocolError(f"V clean of tile {j} finds stage holding {self.vstage[s]}")
+                yield ("step",)
+                self.vstage_users[s].discard("clean")
+                self.V_READY[s].arrive(self)
+
+    def softmax(self, i):
+        self.Q_READY.arrive(self)
+        if i >= self.nq:
+            return
+        yield ("step",)
+        for j in range(self.n):
+            buf = i if self.nq == 2 else (j & 1)
+            e = j if self.nq == 2 else (j >> 1)
+            yield ("wait", self.S_FULL[buf], e)
+            if self.s_buf.get(buf) != ("S", j):
+                raise ProtocolError(f"softmax{i} reads S{buf} for tile {j}, holds {self.s_buf.get(buf)}")
+            self.read_slot(j, f"softmax{i}")
+            yield ("step",)
+            if self.nq == 1 and j > 0:
+                yield ("wait", self.PV_DONE, j - 1)
+            self.read_slot(j, f"softmax{i}-mask")
+            self.s_buf[buf] = ("P", j)
+            self.P_FULL[buf].arrive(self)
+        yield ("wait", self.FINAL, 0)
+
+    def mma(self):
+        n, nq = self.n, self.nq
+        yield ("wait", self.Q_READY, 0)
+        cleaned = [0, 0]
+
+        def wait_v(jj, clean):
+            s = jj % 2
+            yield ("wait", self.V_FULL[s], jj // 2)
+            if clean:
+                yield ("wait", self.V_READY[s], cleaned[s])
+                cleaned[s] += 1
+
+        if nq == 1:
+            cl = [False, False]
+
+            def qk1(j):
+                yield ("wait", self.K_READY[j % 2], j // 2)
+                self.read_slot(j, "mma-qk1")
+                cl[j & 1] = self.clean_of(j)
+                self.qk(0, j, j & 1)
+                self.commit(self.S_FULL[j & 1])
+                self.commit(self.K_FREE[j % 2])
+
+            yield from qk1(0)
+            if n > 1:
+                yield from qk1(1)
+            for j in range(n):
+                yield ("wait", self.P_FULL[j & 1], j >> 1)
+                yield from wait_v(j, cl[j & 1])
+                self.pv(0, j, j & 1)
+                self.commit(self.PV_DONE)
+                self.commit(self.V_FREE[j % 2])
+                if j + 2 < n:
+                    yield from qk1(j + 2)
+        else:
+            yield ("wait", self.K_READY[0], 0)
+            self.read_slot(0, "mma-qk")
+            clean_prev = self.clean_of(0)
+            self.qk(0, 0, 0)
+            self.commit(self.S_FULL[0])
+            self.qk(1, 0, 1)
+            self.commit(self.S_FULL[1])
+            self.commit(self.K_FREE[0])
+            for j in range(1, n):
+                s, sp = j % 2, (j - 1) % 2
+                yield ("wait", self.P_FULL[0], j - 1)
+                yield from wait_v(j - 1, clean_prev)
+                self.pv(0, j - 1, 0)
+                yield ("wait", self.K_READY[s], j // 2)
+                self.read_slot(j, "mma-qk")
+                clean_j = self.clean_of(j)
+                self.qk(0, j, 0)
+                self.commit(self.S_FULL[0])
+                yield ("wait", self.P_FULL[1], j - 1)
+                self.pv(1, j - 1, 1)
+                self.commit(self.V_FREE[sp])
+                self.qk(1, j, 1)
+                self.commit(self.S_FULL[1])
+                self.commit(self.K_FREE[s])
+                clean_prev = clean_j
+            jl = n - 1
+            yield ("wait", self.P_FULL[0], jl)
+            yield from wait_v(jl, clean_prev)
+            self.pv(0, jl, 0)
+            yield ("wait", self.P_FULL[1], jl)
+            self.pv(1, jl, 1)
+            self.commit(self.V_FREE[jl % 2])
+        self.commit(self.FINAL)
+        yield ("wait", self.FINAL, 0)
+
+    # ------------------------------------------------------------------ scheduler
+    def run(self, max_steps=200000):
+        actors = {"producer": self.producer(), "rotation": self.rotation(), "mma": self.mma(),
+                  "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+        state = {name: None for name in actors}  # pending wait or None
+        alive = set(actors)
+        for steps in range(max_steps):
+            runnable = []
+            for name in alive:
+                w = state[name]
+                if w is None:
+                    runnable.append(name)
+                else:
+                    bar, e = w
+                    if bar.k >= e + 2:
+                        raise ProtocolError(f"aliasing: {name} waits {bar.name} phase {e}, barrier at {bar.k}")
+                    if bar.k == e + 1:
+                        runnable.append(name)
+            engines = []
+            if self.tma:
+                engines.append("tma")
+            if self.pipe:
+                engines.append("pipe")
+            if not runnable and not engines:
+                if alive:
+                    raise ProtocolError("deadlock: " + ", ".join(
+                        f"{n} on {state[n][0].name}[{state[n][1]}] (k={state[n][0].k})" for n in sorted(alive)))
+                want = {(i, j) for i in range(self.nq) for j in range(self.n)}
+                if self.done_pv != want or self.done_qk != want:
+                    raise ProtocolError("not every QK^T / PV ran")
+                return steps
+            choice = self.rng.choice(runnable + engines * 2)
+            if choice == "tma":
+                self.step_tma()
+                continue
+            if choice == "pipe":
+                self.step_pipe()
+                continue
+            w = state[choice]
+            if w is not None:
+                w[0].waiters.remove((choice, w[1]))
+            state[choice] = None
+            try:
+                y = next(actors[choice])
+            except StopIteration:
+                alive.discard(choice)
+                continue
+            if y[0] == "wait":
+                state[choice] = (y[1], y[2])
+                y[1].waiters.append((choice, y[2]))
+        raise ProtocolError("step limit")
