@@ -148,6 +148,47 @@ def test_yarn_limits():
     assert abs(lo.yarn_mscale(math.exp(10.0)) - 2.0) < 1e-15
 
 
+@pytest.mark.parametrize("s", [8.0, 4.0, 2.5])
+def test_yarn_ramp_interior_closed_form(s):
+    """Inside the ramp the interpolated frequency is fixed by hand arithmetic.  With
+    rotary_dim = 2 the only frequency is theta_0 = base^0 = 1 (wavelength 2 pi) for any base, so
+    L0 = 33 pi gives r = L0 / lambda = 16.5 and gamma = (16.5 - 1) / (32 - 1) = 1/2, hence
+    theta' = (1/s + 1) / 2; L0 = 17.5 pi gives r = 8.75, gamma = 1/4, theta' = 3/(4s) + 1/4.
+    A ramp divided by beta_fast alone, one that forgets beta_slow, or one that interpolates
+    wavelengths instead of frequencies gives other numbers at both points."""
+    for base in (1e4, 5e5):
+        y = lo.yarn_inv_freq(2, base, s, 33.0 * math.pi, 32.0, 1.0)
+        assert y.shape == (1,)
+        np.testing.assert_allclose(y[0], 0.5 * (1.0 / s + 1.0), rtol=1e-14)
+        y = lo.yarn_inv_freq(2, base, s, 17.5 * math.pi, 32.0, 1.0)
+        np.testing.assert_allclose(y[0], 0.75 / s + 0.25, rtol=1e-14)
+    # rotary_dim = 4, base 4: theta = (1, 1/2), wavelengths (2 pi, 4 pi).  L0 = 66 pi puts pair 0
+    # above beta_fast (r = 33: theta kept) and pair 1 mid-ramp (r = 16.5: gamma = 1/2).
+    y = lo.yarn_inv_freq(4, 4.0, s, 66.0 * math.pi, 32.0, 1.0)
+    np.testing.assert_allclose(y, [1.0, 0.5 * (0.5 / s + 0.5)], rtol=1e-14)
+    # L0 = pi: r = 1/2 and 1/4, both below beta_slow: every frequency divided by s
+    y = lo.yarn_inv_freq(4, 4.0, s, math.pi, 32.0, 1.0)
+    np.testing.assert_allclose(y, [1.0 / s, 0.5 / s], rtol=1e-14)
+    # other ramp bounds: beta (16, 2), r = 9 -> gamma = (9 - 2) / 14 = 1/2
+    y = lo.yarn_inv_freq(2, 1e4, s, 18.0 * math.pi, 16.0, 2.0)
+    np.testing.assert_allclose(y[0], 0.5 * (1.0 / s + 1.0), rtol=1e-14)
+
+
+def test_yarn_ramp_pins_catch_plausible_slips():
+    """Negative control for the pins above: the slips named there each miss the closed form."""
+    s, theta, lam = 8.0, 1.0, 2.0 * math.pi
+    r = 33.0 * math.pi / lam
+    want = 0.5 * (1.0 / s + 1.0)
+    slips = {
+        "divide by beta_fast": np.clip((r - 1.0) / 32.0, 0, 1),
+        "forget beta_slow": np.clip(r / 31.0, 0, 1),
+    }
+    for name, g in slips.items():
+        assert abs((1 - g) * theta / s + g * theta - want) > 1e-3, name
+    g = 0.5  # interpolating the wavelength instead of the frequency
+    assert abs(2 * math.pi / ((1 - g) * lam * s + g * lam) - want) > 1e-3
+
+
 def test_alibi_slopes_values():
     """2^(-8h/32): h = 1 gives 2^-0.25, h = 32 gives 1/256; the workload's input copy agrees."""
     s = lo.alibi_slopes(32)
