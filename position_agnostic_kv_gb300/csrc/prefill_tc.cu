@@ -16,11 +16,16 @@
 //              when a row's max grows by more than 8), P written back to TMEM over S as bf16.
 //   warps 8-11 K rotation: each staged K tile's page rows rotated by their page's Delta in
 //              place in shared memory (cos/sin rows only per distinct Delta, double-buffered,
-//              reused while consecutive tiles stay inside one document); V rows that hold no
-//              key are zeroed so no stale bits reach the tensor core.
+//              reused while consecutive tiles stay inside one document).
 //   warp 12    producer: unpacks the 64-bit block words of a tile's 8 pages (prefetched one tile
-//              ahead) and issues TMA loads (box 16 rows x 64 columns, 128-byte swizzle) into
-//              2-stage K and V rings.
+//              ahead) and issues TMA loads (box 64 columns x 16 rows of one page, 128-byte
+//              swizzle) into 2-stage K and V rings.  A page with r < 16 rows that hold a key
+//              visible to the CTA (a document's partial last page, or query-segment rows past
+//              the CTA's last token) is loaded from row r - 16: its r key rows land in the
+//              stage's last r rows and the 16 - r rows before them are out of the tensor's
+//              bounds, which TMA fills with zeros.  Bytes past a key are never read, so stale
+//              or never-written cache rows (any bit pattern, NaN included) cannot reach PV,
+//              where a zero weight times NaN would still be NaN.
 //   warp 13    TMEM owner and MMA issuer, in the order QK0(j) QK1(j) | PV0(j) QK0(j+1) PV1(j)
 //              QK1(j+1) | ...: S_i = Q_i K^T (A and B from shared memory) into TMEM, then
 //              O_i += P_i V with P_i read from TMEM (A operand in tensor memory) and V as an
@@ -73,16 +78,17 @@ enum : int {
   B_K_READY = 2,   // [2] K tile rotated (128 arrivals)
   B_K_FREE = 4,    // [2] both QK^T done with the K stage (commit)
   B_V_FULL = 6,    // [2] V tile landed (TMA bytes)
-  B_V_READY = 8,   // [2] key-less V rows cleared (128 arrivals); only tiles that need it
-                   //     complete a phase, so both sides count such tiles per stage
-  B_V_FREE = 10,   // [2] both PV done with the V stage (commit)
-  B_S_FULL = 12,   // [2] per Q tile (one live tile: per S buffer): S written (commit)
-  B_P_FULL = 14,   // [2] per Q tile (one live tile: per S buffer): P in TMEM, O rescaled (128)
-  B_Q_READY = 16,  // both Q tiles prepared (256 arrivals)
-  B_FINAL = 17,    // all MMAs finished (commit)
-  B_PV_DONE = 18,  // one live Q tile only: PV of a tile finished (commit)
-  NBAR = 19
+  B_V_FREE = 8,    // [2] both PV done with the V stage (commit)
+  B_S_FULL = 10,   // [2] per Q tile (one live tile: per S buffer): S written (commit)
+  B_P_FULL = 12,   // [2] per Q tile (one live tile: per S buffer): P in TMEM, O rescaled (128)
+  B_Q_READY = 14,  // both Q tiles prepared (256 arrivals)
+  B_FINAL = 15,    // all MMAs finished (commit)
+  B_PV_DONE = 16,  // one live Q tile only: PV of a tile finished (commit)
+  NBAR = 17
 };
+// Every waiter consumes every phase of the barriers it waits on, in order: a parity wait
+// (mbarrier.try_wait.parity) cannot tell the phase it asks for from the one two phases
+// earlier, so waiting on a later phase while an earlier one is still open passes at once.
 
 template <int D>
 struct Layout {
@@ -93,12 +99,13 @@ struct Layout {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + kQT * QTILE;        // K ring
   static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
-  static constexpr int PSTART_OFF = V_OFF + kStages * TILE;  // int [slot][8] first key position per page
+  static constexpr int PSTART_OFF = V_OFF + kStages * TILE;  // int [slot][8] key position of stage row 0
   static constexpr int RUN_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int [slot][8] first page of
                                                                          // the page's run of equal Delta
-  static constexpr int PINFO_OFF = RUN_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, rows}
-  static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, clean}
-  static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] physical pages
+  static constexpr int PINFO_OFF = RUN_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, lo}:
+                                                                         // stage rows [lo, 16) hold keys
+  static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, unused}
+  static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] page * Hkv + head
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
   static constexpr int CS_OFF = TURNS_OFF + (D / 2) * 8;                // float2 [2][8][D/2]
   static constexpr int CS_BUF = kPagesPerTile * (D / 4);                 // float4 per buffer
@@ -189,10 +196,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// 3-D tiled load (column x, row y inside the page, page-head z).  y may be negative: the rows of
+// the box before row 0 are outside the tensor and arrive as zeros; the transaction still
+// counts the whole box.  x is always a multiple of 64 elements (128 bytes).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
@@ -311,7 +321,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       mbar_init(BAR(B_K_READY + s), 128);
       mbar_init(BAR(B_K_FREE + s), 1);
       mbar_init(BAR(B_V_FULL + s), 1);
-      mbar_init(BAR(B_V_READY + s), 128);
       mbar_init(BAR(B_V_FREE + s), 1);
     }
     for (int i = 0; i < kQT; ++i) {
@@ -454,18 +463,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             for (int t = 0; t < kPage; ++t)
               v[pp * kPage + t] = __float_as_uint(__uint_as_float(v[pp * kPage + t]) + fmaf(slope, float(t), base));
           }
-        } else if (!fast) {  // key p = start + t of a page is visible iff t < rows and p <= m
+        } else if (!fast) {  // stage row t of a page holds key p = pstart + t; visible iff t >= lo, p <= m
 #pragma unroll
           for (int pp = 0; pp < kPagesPerTile; ++pp) {
             const int st = pstart[slot * kPagesPerTile + pp];
-            const int lim = min(pinfo[slot * kPagesPerTile + pp].y, m_row - st + 1);
+            const int lo = pinfo[slot * kPagesPerTile + pp].y;
+            const int hi = m_row - st + 1;
             float base = 0.f;
             if constexpr (POS == kAlibi) base = slope * float(st - m_row);
 #pragma unroll
             for (int t = 0; t < kPage; ++t) {
               float x = __uint_as_float(v[pp * kPage + t]);
               if constexpr (POS == kAlibi) x += fmaf(slope, float(t), base);
-              v[pp * kPage + t] = __float_as_uint(t < lim ? x : -INFINITY);
+              v[pp * kPage + t] = __float_as_uint((t >= lo && t < hi) ? x : -INFINITY);
             }
           }
         }
@@ -559,7 +569,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       }
     }
   } else if (warp < kProdWarp) {
-    // ============================ K rotation, V cleaning
+    // ============================ K rotation
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::rot));
     const int rt = threadIdx.x - kRotWarp0 * 32;
     const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
@@ -572,7 +582,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       const int s = j % kStages, slot = j % kSlots;
       const uint32_t par = uint32_t((j / kStages) & 1);
       if (ok) ok = wait_bar(BAR(B_K_FULL + s), par, abort_flag, a.status);
-      const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, rows}
+      const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, lo}
       if constexpr (kRotate) {
         const uint32_t sK = sK0 + uint32_t(s * L::TILE);
         // cos/sin rows only for pages that start a new document offset: page pp uses the row of
@@ -594,7 +604,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           }
         }
         named_sync(1, 128);
-        if (ok && t < pi.y) {
+        if (ok && t >= pi.y) {  // rows before lo hold zeros (no key)
           const float4* c4 = cs4 + cs_buf * L::CS_BUF + run_start * (D / 4);
           const int rd = a.pos.rotary_dim;
           if (rd == D && !a.pos.interleaved) {  // full half-split rotation (the common case)
@@ -670,22 +680,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         fence_async_smem();
       }
       mbar_arrive(BAR(B_K_READY + s));
-      // V: rows holding no key are cleared so no stale bits reach the tensor core.  Waiting for
-      // this tile's V also means the previous PV on this stage is done, so V_READY can never run
-      // two phases ahead of the MMA thread.
-      const bool clean = flags[slot * 2 + 1] != 0;
-      if (clean) {
-        if (ok) ok = wait_bar(BAR(B_V_FULL + s), par, abort_flag, a.status);
-        if (ok && t >= pi.y) {
-          const uint32_t sV = sV0 + uint32_t(s * L::TILE);
-#pragma unroll
-          for (int cb = 0; cb < L::CB; ++cb)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(rt, c), make_uint4(0, 0, 0, 0));
-        }
-        fence_async_smem();
-        mbar_arrive(BAR(B_V_READY + s));
-      }
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::issue));
@@ -711,54 +705,56 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const int s = j % kStages, slot = j % kSlots;
         const uint64_t w = w_next;
         w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
+        // rows: keys of the page that some row of this CTA may see.  Only a document's last page
+        // is partial (a prefix of n_valid rows); in the query segment the rows past the CTA's
+        // last token m_max are not needed (and may not be written yet).
         int rows = 0, start = 0, page = 0, delta = 0;
         const int jb = tile_of(j) * kPagesPerTile + lane;
         if (lane < kPagesPerTile && jb < nb) {
           page = int(word_page(w));
           delta = int(word_delta(w));
           start = delta + kPage * int(word_pg(w));
-          rows = min(int(word_nvalid(w)), kPage);
+          rows = max(0, min(min(int(word_nvalid(w)), kPage), m_max - start + 1));
           if (page >= a.num_pages) {
             set_status(a.status, LAZY_STATUS_BAD_PAGE);
             rows = 0;
           }
         }
+        const int lo = kPage - rows;  // the page is loaded from row -lo: stage rows [lo, 16) hold its keys
         if (j >= kStages) {
           const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
           if (!__all_sync(0xffffffffu, freed)) return false;
         }
         const int prev_delta = __shfl_up_sync(0xffffffffu, delta, 1);
         const uint32_t runs = __ballot_sync(0xffffffffu, lane >= 1 && lane < kPagesPerTile && delta != prev_delta);
+        const int zc = page * a.Hkv + g;  // page-head coordinate of the tensor map
         if (lane < kPagesPerTile) {
-          pinfo[slot * kPagesPerTile + lane] = make_int2(delta, rows);
-          pgid[slot * kPagesPerTile + lane] = rows > 0 ? page : -1;
-          pstart[slot * kPagesPerTile + lane] = start;
+          pinfo[slot * kPagesPerTile + lane] = make_int2(delta, lo);
+          pgid[slot * kPagesPerTile + lane] = rows > 0 ? zc : -1;
+          pstart[slot * kPagesPerTile + lane] = start - lo;
           const uint32_t upto = runs & ((2u << lane) - 1u);  // run starts at or before this page
           prun[slot * kPagesPerTile + lane] = upto ? 31 - __clz(upto) : 0;
         }
         const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
         const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
-        if (lane == 0) {
-          flags[slot * 2] = all16 && (last_start + kPage - 1 <= m_min);  // every key visible to every row
-          flags[slot * 2 + 1] = !all16;                                  // some V rows must be cleared
-        }
+        if (lane == 0) flags[slot * 2] = all16 && (last_start + kPage - 1 <= m_min);  // every key visible to every row
         __syncwarp();
-        uint32_t bytes = 0;
-        for (int pp = 0; pp < kPagesPerTile; ++pp)
-          if (__shfl_sync(0xffffffffu, rows, pp) > 0) bytes += uint32_t(kPage) * D * 2;
+        const uint32_t loaded = __ballot_sync(0xffffffffu, lane < kPagesPerTile && rows > 0);
+        const uint32_t bytes = uint32_t(__popc(loaded)) * kPage * D * 2;  // whole boxes, zero rows included
         const uint32_t sK = sK0 + uint32_t(s * L::TILE);
         if (lane == 0) mbar_arrive_expect_tx(BAR(B_K_FULL + s), bytes);
         __syncwarp();
         if (lane < kPagesPerTile && rows > 0)  // one lane per page: TMA issue is per-instruction bound
 #pragma unroll
           for (int cb = 0; cb < L::CB; ++cb)
-            tma_load_2d(sK + uint32_t(cb * L::BLK + lane * kPage * 128), &tmk, cb * 64, (page * a.Hkv + g) * kPage,
-                        BAR(B_K_FULL + s));
+            tma_load_3d(sK + uint32_t(cb * L::BLK + lane * kPage * 128), &tmk, cb * 64, -lo, zc, BAR(B_K_FULL + s));
         __syncwarp();
         issued_k = j + 1;
         return true;
       };
-      // V of tile j (its metadata was published with its K)
+      // V of tile j (its metadata was published with its K).  A page slot past the CTA's last
+      // block gets no load; its stage rows still meet the PV MMA (with zero weights), so they are
+      // cleared here, after the stage's previous PV is done, instead of keeping stale bits.
       auto issue_v = [&](int j) -> bool {
         const int s = j % kStages, slot = j % kSlots;
         if (j >= kStages) {
@@ -766,15 +762,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           if (!__all_sync(0xffffffffu, freed)) return false;
         }
         const uint32_t sV = sV0 + uint32_t(s * L::TILE);
-        const int pg_id = lane < kPagesPerTile ? pgid[slot * kPagesPerTile + lane] : -1;
-        const uint32_t bytes = uint32_t(__popc(__ballot_sync(0xffffffffu, pg_id >= 0))) * kPage * D * 2;
-        if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), bytes);
+        const int zc = lane < kPagesPerTile ? pgid[slot * kPagesPerTile + lane] : -1;
+        const int lo = lane < kPagesPerTile ? pinfo[slot * kPagesPerTile + lane].y : kPage;
+        const uint32_t loaded = __ballot_sync(0xffffffffu, zc >= 0);
+        const uint32_t empty = ~loaded & ((1u << kPagesPerTile) - 1u);
+        if (empty) {  // a warp-wide store of 16 B per lane covers two rows of a column block
+          for (int pp = 0; pp < kPagesPerTile; ++pp) {
+            if (!((empty >> pp) & 1u)) continue;
+#pragma unroll
+            for (int cb = 0; cb < L::CB; ++cb)
+#pragma unroll
+              for (int i = 0; i < kPage * 8 / 32; ++i) {
+                const int row = pp * kPage + (i * 32 + lane) / 8, c = (i * 32 + lane) % 8;
+                st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(row, c), make_uint4(0, 0, 0, 0));
+              }
+          }
+          fence_async_smem();
+        }
         __syncwarp();
-        if (pg_id >= 0)
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), uint32_t(__popc(loaded)) * kPage * D * 2);
+        __syncwarp();
+        if (zc >= 0)
 #pragma unroll
           for (int cb = 0; cb < L::CB; ++cb)
-            tma_load_2d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, (pg_id * a.Hkv + g) * kPage,
-                        BAR(B_V_FULL + s));
+            tma_load_3d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, -lo, zc, BAR(B_V_FULL + s));
         __syncwarp();
         issued_v = j + 1;
         return true;
@@ -805,7 +816,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         constexpr uint32_t IQK = idesc_mma(kM, kN, 0, kQkF16 ? 1 : 0);
         constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
         bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
-        int cleaned[kStages] = {0, 0};  // V_READY phases consumed per stage
         auto qk = [&](int qt, int j) {  // S_qt = Q_qt K_j^T
           const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE), sQ = sQ0 + uint32_t(qt * L::QTILE);
 #pragma unroll
@@ -823,24 +833,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             mma_ts(tmem + uint32_t(2 * kN + qt * 128), tmem + uint32_t(qt * kN + kk * 8),
                    sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (jj > 0 || kk > 0) ? 1u : 0u);
         };
-        auto wait_v = [&](int jj, bool clean) -> bool {
-          const int s = jj % kStages;
-          if (!wait_bar(BAR(B_V_FULL + s), uint32_t((jj / kStages) & 1), abort_flag, a.status)) return false;
-          if (clean) {
-            if (!wait_bar(BAR(B_V_READY + s), uint32_t(cleaned[s] & 1), abort_flag, a.status)) return false;
-            ++cleaned[s];
-          }
-          return true;
+        auto wait_v = [&](int jj) -> bool {  // every V_FULL phase of both stages, in tile order
+          return wait_bar(BAR(B_V_FULL + jj % kStages), uint32_t((jj / kStages) & 1), abort_flag, a.status);
         };
-        bool clean_prev = false;  // clean flag of the tile whose PV is issued next
         if (nq == 1) {
           // one live Q tile: tile j's scores in S_{j%2}; order QK(0) QK(1) | PV(0) QK(2) | PV(1) ...
-          bool clean[2] = {false, false};  // clean flags of the tiles whose QK is issued, by j % 2
           auto qk1 = [&](int j) -> bool {
             if (!wait_bar(BAR(B_K_READY + j % kStages), uint32_t((j / kStages) & 1), abort_flag, a.status))
               return false;
             tc_fence_after();
-            clean[j & 1] = flags[(j % kSlots) * 2 + 1] != 0;
             const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -856,7 +857,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           if (ok && ntiles > 1) ok = qk1(1);
           for (int j = 0; j < ntiles && ok; ++j) {
             ok = wait_bar(BAR(B_P_FULL + (j & 1)), uint32_t((j >> 1) & 1), abort_flag, a.status) &&
-                 wait_v(j, clean[j & 1]);
+                 wait_v(j);
             if (!ok) break;
             tc_fence_after();
             const uint32_t sV = sV0 + uint32_t((j % kStages) * L::TILE);
@@ -873,14 +874,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (ok) ok = wait_bar(BAR(B_K_READY), 0, abort_flag, a.status);
         if (ok) {
           tc_fence_after();
-          clean_prev = flags[1] != 0;  // published before K_FULL of tile 0
           qk(0, 0);
           if (nq == 2) qk(1, 0);
           mma_commit(BAR(B_K_FREE));
         }
         for (int j = 1; j < ntiles && ok; ++j) {
           const int s = j % kStages, sp = (j - 1) % kStages;
-          if (!wait_bar(BAR(B_P_FULL), uint32_t((j - 1) & 1), abort_flag, a.status) || !wait_v(j - 1, clean_prev)) {
+          if (!wait_bar(BAR(B_P_FULL), uint32_t((j - 1) & 1), abort_flag, a.status) || !wait_v(j - 1)) {
             ok = false;
             break;
           }
@@ -891,7 +891,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             break;
           }
           tc_fence_after();
-          const bool clean_j = flags[(j % kSlots) * 2 + 1] != 0;
           qk(0, j);
           if (nq == 2) {
             if (!wait_bar(BAR(B_P_FULL + 1), uint32_t((j - 1) & 1), abort_flag, a.status)) {
@@ -904,11 +903,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           mma_commit(BAR(B_V_FREE + sp));
           if (nq == 2) qk(1, j);
           mma_commit(BAR(B_K_FREE + s));
-          clean_prev = clean_j;
         }
         if (ok) {
           const int jl = ntiles - 1;
-          ok = wait_bar(BAR(B_P_FULL), uint32_t(jl & 1), abort_flag, a.status) && wait_v(jl, clean_prev);
+          ok = wait_bar(BAR(B_P_FULL), uint32_t(jl & 1), abort_flag, a.status) && wait_v(jl);
           if (ok) {
             tc_fence_after();
             pv(0, jl);
@@ -963,16 +961,18 @@ static EncodeTiledFn encoder() {
   return fn;
 }
 
-// Tensor map of a paged cache viewed as rows = num_pages * Hkv * 16, columns = D (bf16); one
-// TMA box = 16 rows (one page of one head) x 64 columns, 128-byte swizzle.
+// Tensor map of a paged cache as a 3-D tensor: columns (D, bf16) x rows of a page (16) x
+// page-heads (num_pages * Hkv).  One TMA box = 64 columns x 16 rows x 1 page-head with the
+// 128-byte swizzle.  Rows outside [0, 16) of a page are outside the tensor and read as zero
+// (FLOAT_OOB_FILL_NONE), so a box started at a negative row zero-fills the rows before row 0.
 static int cache_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int D) {
   EncodeTiledFn enc = encoder();
   if (!enc) return fail(LAZY_ECUDA, "cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(num_pages) * cuuint64_t(Hkv) * kPage};
-  const cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-  const cuuint32_t box[2] = {64, kPage};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(kPage), cuuint64_t(num_pages) * cuuint64_t(Hkv)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(kPage) * D * 2};
+  const cuuint32_t box[3] = {64, kPage, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(LAZY_ECUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));

@@ -1,15 +1,27 @@
 """Discrete-event model of the tensor-core attention kernel's mbarrier protocol (test
 infrastructure, host only).
 
-The roles of prefill_tc_kernel (K/V producer, K rotation and V cleaning, softmax of each Q tile,
-MMA issuer) are generators that yield ('wait', barrier, phase) or ('step',), in the same order
-of waits, arrivals and commits as the kernel, for both schedules (two live Q tiles, and one live
-Q tile whose scores alternate between the two S buffers).  Asynchronous engines: TMA copies land
-in any order; the tensor pipe runs MMAs in issue order and a commit arrives once every earlier
-MMA is done.  A random scheduler interleaves everything.  Checked: no deadlock; no parity
-aliasing (a barrier completing two phases past a waiter's, which try_wait.parity cannot tell
-apart); no metadata slot overwritten while a reader still needs it; no K/V stage refilled
-before all its consumers are done; S/P tensor-memory buffers written in a safe order.
+The roles of prefill_tc_kernel (K/V producer, K rotation, softmax of each Q tile, MMA issuer)
+are generators that yield ('wait', barrier, phase) or ('step',), in the same order of waits,
+arrivals and commits as the kernel, for both schedules (two live Q tiles, and one live Q tile
+whose scores alternate between the two S buffers).  Asynchronous engines: TMA copies land in
+any order, each after a random latency (in scheduler steps; the bound is drawn per run, up to
+tens of steps, so that a copy can stay in flight while the roles run several tiles ahead); the
+tensor pipe runs MMAs in issue order and a commit arrives once every earlier MMA is done.  A
+random scheduler interleaves everything.
+
+Waits follow mbarrier.try_wait.parity exactly.  A wait for phase e of a barrier that has
+completed k phases passes iff k - e is odd: besides the intended k = e + 1 it also passes when
+the waiter is AHEAD of the barrier (k = e - 1, e - 3, ...: the phase asked for has not even
+begun), and it blocks when the barrier is two phases past (k = e + 2: aliasing).  The model
+raises on both: on any waiter registered while k < e, and on any k >= e + 2.
+
+Checked besides: no deadlock; no metadata slot overwritten while a reader still needs it; no
+K/V stage refilled before all its consumers are done; S/P tensor-memory buffers written in a
+safe order; every QK^T and PV runs exactly once.
+
+Subclasses may override the hooks (``v_users``, ``rotation``, ``mma_wait_v``, ``mma_saw``,
+``producer``, ``softmax``) to plant a protocol mistake that the checks must catch.
 """
 import random
 
@@ -22,57 +34,55 @@ class Bar:
     def __init__(self, name, need):
         self.name, self.need = name, need
         self.arr, self.tx, self.k = 0, 0, 0
-        self.waiters = []  # (actor, phase)
 
-    def _check(self, sim):
+    def _check(self):
         if self.arr == self.need and self.tx == 0:
             self.arr = 0
             self.k += 1
-            for a, e in self.waiters:
-                if e < self.k - 1:
-                    raise ProtocolError(f"aliasing on {self.name}: waiter {a} wants phase {e}, barrier at {self.k}")
 
-    def arrive(self, sim, expect_tx=0):
+    def arrive(self, expect_tx=0):
         self.arr += 1
         self.tx += expect_tx
         if self.arr > self.need:
             raise ProtocolError(f"{self.name}: too many arrivals")
-        self._check(sim)
+        self._check()
 
-    def complete_tx(self, sim, b):
+    def complete_tx(self, b):
         self.tx -= b
-        self._check(sim)
+        self._check()
 
 
 class Sim:
-    def __init__(self, ntiles, nq, clean, seed=0, slots=4):
+    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4):
+        """ntiles K/V tiles, nq live Q tiles (1 or 2), `clean(j)`: whether tile j has key-less
+        rows (used only by subclasses that model a V-cleaning role)."""
         self.rng = random.Random(seed)
-        self.n, self.nq, self.clean_of = ntiles, nq, clean
+        self.now = 0
+        self.max_latency = self.rng.choice([0, 3, 12, 40])
+        self.n, self.nq = ntiles, nq
+        self.clean_of = clean or (lambda j: False)
         self.slots = slots
-        B = lambda name, need: Bar(name, need)
-        self.K_FULL = [B(f"K_FULL{s}", 1) for s in range(2)]
-        self.K_READY = [B(f"K_READY{s}", 1) for s in range(2)]
-        self.K_FREE = [B(f"K_FREE{s}", 1) for s in range(2)]
-        self.V_FULL = [B(f"V_FULL{s}", 1) for s in range(2)]
-        self.V_READY = [B(f"V_READY{s}", 1) for s in range(2)]
-        self.V_FREE = [B(f"V_FREE{s}", 1) for s in range(2)]
-        self.S_FULL = [B(f"S_FULL{i}", 1) for i in range(2)]
-        self.P_FULL = [B(f"P_FULL{i}", 1) for i in range(2)]
-        self.PV_DONE = B("PV_DONE", 1)
-        self.Q_READY = B("Q_READY", 2)
-        self.FINAL = B("FINAL", 1)
+        self.K_FULL = [Bar(f"K_FULL{s}", 1) for s in range(2)]
+        self.K_READY = [Bar(f"K_READY{s}", 1) for s in range(2)]
+        self.K_FREE = [Bar(f"K_FREE{s}", 1) for s in range(2)]
+        self.V_FULL = [Bar(f"V_FULL{s}", 1) for s in range(2)]
+        self.V_FREE = [Bar(f"V_FREE{s}", 1) for s in range(2)]
+        self.S_FULL = [Bar(f"S_FULL{i}", 1) for i in range(2)]
+        self.P_FULL = [Bar(f"P_FULL{i}", 1) for i in range(2)]
+        self.PV_DONE = Bar("PV_DONE", 1)
+        self.Q_READY = Bar("Q_READY", 2)
+        self.FINAL = Bar("FINAL", 1)
         # state for hazard checks
         self.slot_tile = [None] * self.slots
-        self.kstage = [None, None]      # tile whose K is in the stage (landed)
+        self.kstage = [None, None]          # tile whose K is in the stage (landed)
         self.vstage = [None, None]
         self.kstage_users = [set(), set()]  # outstanding consumers of the stage's tile
         self.vstage_users = [set(), set()]
-        self.tma = []      # pending copies: (kind, stage, tile, bar, tx)
+        self.tma = []      # pending copies: (kind, stage, tile, bar, earliest landing step)
         self.pipe = []     # tensor pipe FIFO: ('mma', fn) or ('commit', bar)
-        self.s_buf = {}    # S/P buffer -> ('S', tile) / ('P', tile) for hazard checks
+        self.s_buf = {}    # S/P buffer -> ('S', tile) / ('P', tile)
         self.done_qk = set()
         self.done_pv = set()
-        self.p_written = set()
 
     # ------------------------------------------------------------------ hazards
     def read_slot(self, j, who):
@@ -81,53 +91,55 @@ class Sim:
             raise ProtocolError(f"{who} reads slot {s} for tile {j}, holds {self.slot_tile[s]}")
 
     def publish(self, j):
-        s = j % self.slots
-        self.slot_tile[s] = j
+        self.slot_tile[j % self.slots] = j
+
+    def v_users(self, j):
+        """Consumers of a landed V tile."""
+        return {"pv0"} | ({"pv1"} if self.nq == 2 else set())
 
     # ------------------------------------------------------------------ engines
-    def issue_tma(self, kind, j, bar, tx=1):
+    def issue_tma(self, kind, j, bar):
         st = j % 2
         users = self.kstage_users[st] if kind == "K" else self.vstage_users[st]
         if users:
             raise ProtocolError(f"{kind}({j}) issued into stage {st} while {sorted(users)} still use it")
-        self.tma.append((kind, st, j, bar))
+        self.tma.append((kind, st, j, bar, self.now + self.rng.randint(0, self.max_latency)))
+
+    def tma_ready(self):
+        return [i for i, c in enumerate(self.tma) if c[4] <= self.now]
 
     def step_tma(self):
-        if not self.tma:
-            return False
-        i = self.rng.randrange(len(self.tma))
-        kind, st, j, bar = self.tma.pop(i)
+        i = self.rng.choice(self.tma_ready())
+        kind, st, j, bar, _ = self.tma.pop(i)
         if kind == "K":
             self.kstage[st] = j
             self.kstage_users[st] = {"rot", "qk0"} | ({"qk1"} if self.nq == 2 else set())
         else:
             self.vstage[st] = j
-            self.vstage_users[st] = {"pv0"} | ({"pv1"} if self.nq == 2 else set()) | (
-                {"clean"} if self.clean_of(j) else set())
-        bar.complete_tx(self, 1)
-        return True
+            self.vstage_users[st] = self.v_users(j)
+        bar.complete_tx(1)
 
     def step_pipe(self):
-        if not self.pipe:
-            return False
         op = self.pipe.pop(0)
         if op[0] == "commit":
-            op[1].arrive(self)
+            op[1].arrive()
         else:
             op[1]()
-        return True
 
     # ------------------------------------------------------------------ MMAs
     def qk(self, i, j, buf):
         def run():
             st = j % 2
             if self.kstage[st] != j or "rot" in self.kstage_users[st]:
-                raise ProtocolError(f"QK{i}({j}) reads K stage {st} holding {self.kstage[st]} (rotated: {'rot' not in self.kstage_users[st]})")
+                raise ProtocolError(f"QK{i}({j}) reads K stage {st} holding {self.kstage[st]} "
+                                    f"(rotated: {'rot' not in self.kstage_users[st]})")
             prev = self.s_buf.get(buf)
             if prev is not None and prev[0] == "P" and (i, prev[1]) not in self.done_pv:
                 raise ProtocolError(f"QK{i}({j}) overwrites P({prev[1]}) in S{buf} before its PV")
             if prev is not None and prev[0] == "S":
                 raise ProtocolError(f"QK{i}({j}) overwrites S({prev[1]}) in S{buf} before the softmax read it")
+            if (i, j) in self.done_qk:
+                raise ProtocolError(f"QK{i}({j}) runs twice")
             self.s_buf[buf] = ("S", j)
             self.kstage_users[st].discard(f"qk{i}")
             self.done_qk.add((i, j))
@@ -136,10 +148,14 @@ class Sim:
     def pv(self, i, j, buf):
         def run():
             st = j % 2
-            if self.vstage[st] != j or "clean" in self.vstage_users[st]:
-                raise ProtocolError(f"PV{i}({j}) reads V stage {st} holding {self.vstage[st]}")
+            others = self.vstage_users[st] - {"pv0", "pv1"}
+            if self.vstage[st] != j or others:
+                raise ProtocolError(f"PV{i}({j}) reads V stage {st} holding {self.vstage[st]} "
+                                    f"(still pending: {sorted(others)})")
             if self.s_buf.get(buf) != ("P", j):
                 raise ProtocolError(f"PV{i}({j}) reads S{buf} holding {self.s_buf.get(buf)}")
+            if (i, j) in self.done_pv:
+                raise ProtocolError(f"PV{i}({j}) runs twice")
             self.vstage_users[st].discard(f"pv{i}")
             self.done_pv.add((i, j))
         self.pipe.append(("mma", run))
@@ -156,16 +172,16 @@ class Sim:
             if j >= 2:
                 yield ("wait", self.K_FREE[s], j // 2 - 1)
             self.publish(j)
-            self.K_FULL[s].arrive(self, expect_tx=1)
+            self.K_FULL[s].arrive(expect_tx=1)
             self.issue_tma("K", j, self.K_FULL[s])
             yield ("step",)
 
-        def issue_v(j):
+        def issue_v(j):  # wait for the stage; clear empty page slots; load V
             s = j % 2
             if j >= 2:
                 yield ("wait", self.V_FREE[s], j // 2 - 1)
             self.read_slot(j, "issue_v")
-            self.V_FULL[s].arrive(self, expect_tx=1)
+            self.V_FULL[s].arrive(expect_tx=1)
             self.issue_tma("V", j, self.V_FULL[s])
             yield ("step",)
 
@@ -185,18 +201,10 @@ class Sim:
             if self.kstage[s] != j:
                 raise ProtocolError(f"rotation of K({j}) finds stage holding {self.kstage[s]}")
             self.kstage_users[s].discard("rot")
-            self.K_READY[s].arrive(self)
-            self.read_slot(j, "rotation-clean")
-            if self.clean_of(j):
-                yield ("wait", self.V_FULL[s], j // 2)
-                if self.vstage[s] != j:
-                    raise ProtocolError(f"V clean of tile {j} finds stage holding {self.vstage[s]}")
-                yield ("step",)
-                self.vstage_users[s].discard("clean")
-                self.V_READY[s].arrive(self)
+            self.K_READY[s].arrive()
 
     def softmax(self, i):
-        self.Q_READY.arrive(self)
+        self.Q_READY.arrive()
         if i >= self.nq:
             return
         yield ("step",)
@@ -212,28 +220,24 @@ class Sim:
                 yield ("wait", self.PV_DONE, j - 1)
             self.read_slot(j, f"softmax{i}-mask")
             self.s_buf[buf] = ("P", j)
-            self.P_FULL[buf].arrive(self)
+            self.P_FULL[buf].arrive()
         yield ("wait", self.FINAL, 0)
+
+    def mma_wait_v(self, jj):
+        """The MMA thread's wait before PV of tile jj: V_FULL of its stage, every phase in order."""
+        yield ("wait", self.V_FULL[jj % 2], jj // 2)
+
+    def mma_saw(self, j):
+        """Hook: the MMA thread has read tile j's metadata slot (just before its QK^T)."""
 
     def mma(self):
         n, nq = self.n, self.nq
         yield ("wait", self.Q_READY, 0)
-        cleaned = [0, 0]
-
-        def wait_v(jj, clean):
-            s = jj % 2
-            yield ("wait", self.V_FULL[s], jj // 2)
-            if clean:
-                yield ("wait", self.V_READY[s], cleaned[s])
-                cleaned[s] += 1
-
         if nq == 1:
-            cl = [False, False]
-
             def qk1(j):
                 yield ("wait", self.K_READY[j % 2], j // 2)
                 self.read_slot(j, "mma-qk1")
-                cl[j & 1] = self.clean_of(j)
+                self.mma_saw(j)
                 self.qk(0, j, j & 1)
                 self.commit(self.S_FULL[j & 1])
                 self.commit(self.K_FREE[j % 2])
@@ -243,7 +247,7 @@ class Sim:
                 yield from qk1(1)
             for j in range(n):
                 yield ("wait", self.P_FULL[j & 1], j >> 1)
-                yield from wait_v(j, cl[j & 1])
+                yield from self.mma_wait_v(j)
                 self.pv(0, j, j & 1)
                 self.commit(self.PV_DONE)
                 self.commit(self.V_FREE[j % 2])
@@ -252,7 +256,7 @@ class Sim:
         else:
             yield ("wait", self.K_READY[0], 0)
             self.read_slot(0, "mma-qk")
-            clean_prev = self.clean_of(0)
+            self.mma_saw(0)
             self.qk(0, 0, 0)
             self.commit(self.S_FULL[0])
             self.qk(1, 0, 1)
@@ -261,11 +265,11 @@ class Sim:
             for j in range(1, n):
                 s, sp = j % 2, (j - 1) % 2
                 yield ("wait", self.P_FULL[0], j - 1)
-                yield from wait_v(j - 1, clean_prev)
+                yield from self.mma_wait_v(j - 1)
                 self.pv(0, j - 1, 0)
                 yield ("wait", self.K_READY[s], j // 2)
                 self.read_slot(j, "mma-qk")
-                clean_j = self.clean_of(j)
+                self.mma_saw(j)
                 self.qk(0, j, 0)
                 self.commit(self.S_FULL[0])
                 yield ("wait", self.P_FULL[1], j - 1)
@@ -274,10 +278,9 @@ class Sim:
                 self.qk(1, j, 1)
                 self.commit(self.S_FULL[1])
                 self.commit(self.K_FREE[s])
-                clean_prev = clean_j
             jl = n - 1
             yield ("wait", self.P_FULL[0], jl)
-            yield from wait_v(jl, clean_prev)
+            yield from self.mma_wait_v(jl)
             self.pv(0, jl, 0)
             yield ("wait", self.P_FULL[1], jl)
             self.pv(1, jl, 1)
@@ -286,28 +289,36 @@ class Sim:
         yield ("wait", self.FINAL, 0)
 
     # ------------------------------------------------------------------ scheduler
+    def actors(self):
+        return {"producer": self.producer(), "rotation": self.rotation(), "mma": self.mma(),
+                "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+
     def run(self, max_steps=200000):
-        actors = {"producer": self.producer(), "rotation": self.rotation(), "mma": self.mma(),
-                  "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
-        state = {name: None for name in actors}  # pending wait or None
+        actors = self.actors()
+        state = {name: None for name in actors}  # pending (barrier, phase) or None
         alive = set(actors)
         for steps in range(max_steps):
+            self.now += 1
             runnable = []
-            for name in alive:
+            for name in sorted(alive):
                 w = state[name]
                 if w is None:
                     runnable.append(name)
-                else:
-                    bar, e = w
-                    if bar.k >= e + 2:
-                        raise ProtocolError(f"aliasing: {name} waits {bar.name} phase {e}, barrier at {bar.k}")
-                    if bar.k == e + 1:
-                        runnable.append(name)
-            engines = []
-            if self.tma:
-                engines.append("tma")
-            if self.pipe:
-                engines.append("pipe")
+                    continue
+                bar, e = w
+                if bar.k < e:
+                    raise ProtocolError(
+                        f"waiter ahead: {name} waits {bar.name} phase {e} while the barrier has completed "
+                        f"only {bar.k} phases (a parity wait would "
+                        f"{'pass at once' if (e - bar.k) % 2 else 'pass on the wrong phase'})")
+                if bar.k >= e + 2:
+                    raise ProtocolError(f"aliasing: {name} waits {bar.name} phase {e}, barrier at {bar.k}")
+                if bar.k == e + 1:
+                    runnable.append(name)
+            engines = (["tma"] if self.tma_ready() else []) + (["pipe"] if self.pipe else [])
+            if not runnable and not engines and self.tma:  # only copies in flight: time passes
+                self.now = min(c[4] for c in self.tma)
+                continue
             if not runnable and not engines:
                 if alive:
                     raise ProtocolError("deadlock: " + ", ".join(
@@ -323,9 +334,6 @@ class Sim:
             if choice == "pipe":
                 self.step_pipe()
                 continue
-            w = state[choice]
-            if w is not None:
-                w[0].waiters.remove((choice, w[1]))
             state[choice] = None
             try:
                 y = next(actors[choice])
@@ -334,5 +342,4 @@ class Sim:
                 continue
             if y[0] == "wait":
                 state[choice] = (y[1], y[2])
-                y[1].waiters.append((choice, y[2]))
         raise ProtocolError("step limit")

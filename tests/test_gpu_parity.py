@@ -22,9 +22,24 @@ def lk():
     return lib()
 
 
-def _batch(w, **kw):
+NAN_BITS = 0x7FC0  # a quiet-NaN bf16 pattern
+
+
+def _batch(w, poison=False, **kw):
+    """A PagedBatch; with poison=True every cache row starts as NaN bits, so any row the kernels
+    read without a key written there (past a document's end, past the causal frontier, or a
+    page slot past the last block) would turn the output into NaN."""
     from position_agnostic_kv_gb300.runner import PagedBatch
-    return PagedBatch(w, device="cuda", **kw)
+    pb = PagedBatch(w, device="cuda", **kw)
+    if poison:
+        pb.k_cache.view(torch_int16()).fill_(NAN_BITS)
+        pb.v_cache.view(torch_int16()).fill_(NAN_BITS)
+    return pb
+
+
+def torch_int16():
+    import torch
+    return torch.int16
 
 
 def _bits(t):
@@ -84,11 +99,13 @@ def test_kv_write_parity(lk, name):
 
 
 # ------------------------------------------------------------------ attention
-def _run_and_check(lk, w, reqs, n_steps, check_steps, use_table=False, sharpen=1.0):
+def _run_and_check(lk, w, reqs, n_steps, check_steps, use_table=False, sharpen=1.0, poison=False,
+                   outputs=None):
     """Run fill -> prefill -> n_steps decode steps on the GPU; compare prefill rows of `reqs`
-    and the decode outputs of `reqs` at `check_steps` against the oracle."""
+    and the decode outputs of `reqs` at `check_steps` against the oracle.  `outputs`, a dict,
+    receives the GPU outputs ('prefill' and 'decode<t>' for t in check_steps)."""
     import torch
-    pb = _batch(w, use_table=use_table)
+    pb = _batch(w, use_table=use_table, poison=poison)
     pb.fill_documents()
     inp = pb.upload_prefill()
     if sharpen != 1.0:
@@ -101,6 +118,9 @@ def _run_and_check(lk, w, reqs, n_steps, check_steps, use_table=False, sharpen=1
             outs_d[t] = o.clone()
     torch.cuda.synchronize()
     _status_clean(lk)
+    if outputs is not None:
+        outputs["prefill"] = out_p.clone()
+        outputs.update({f"decode{t}": o for t, o in outs_d.items()})
 
     bt, meta, seq_len, q_start, doc_blocks = oracle_meta(w)
     np.testing.assert_array_equal(meta, pb.meta_h)
@@ -188,10 +208,13 @@ def test_decode32k(lk):
     _run_and_check(lk, w, [0, 21, 42, 63], 128, {0, 63, 127})
 
 
-@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 4), (64, 8, 2), (128, 8, 1), (128, 16, 2), (64, 16, 2)])
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 4, 4), (64, 8, 2), (128, 8, 1), (128, 16, 2), (64, 16, 2),
+                                      (128, 24, 1), (64, 48, 2)])
 def test_edge_shapes(lk, D, Hq, Hkv):
     """Documents of 1, 15, 16, 17 and 33 tokens, uneven query lengths (one request without a
-    query segment), MHA / GQA / MQA groupings and both head dims."""
+    query segment), MHA / GQA / MQA groupings and both head dims.  Head groups of 24 do not
+    divide the tensor-core kernel's 128 rows, so their prefill runs one CUDA-core CTA per query
+    row (the decode kernel's row mode) and their decode takes 8 heads per CTA."""
     w = make_custom([1, 15, 16, 17, 33], [[4, 0, 2], [1, 3], [2, 4, 1, 0]], Hq, Hkv, D,
                     PosCfg("rope", 1e4, D), [3, 0, 17], 5, seed=D + Hq)
     _run_and_check(lk, w, [0, 1, 2], 5, {0, 4})
@@ -355,6 +378,73 @@ def test_sharpened_queries_separate_negative_controls(lk):
         wrong, _ = lo.prefill(q4, w.cu_q, qs, db, bad, kc, vc, pos)
         err = np.abs(out.float().cpu().numpy() - wrong).max()
         assert err > 2e-2, f"negative control not separated: {err:.3e}"
+
+
+# ------------------------------------------------------------------ poisoned caches
+POISON_CASES = {  # name -> (workload, requests checked, decode steps, steps checked)
+    # 32-token queries of a 4-head group: one live Q tile per CTA; 200-token documents end mid-page
+    "rag8b_one_q_tile": (lambda: make_workload("rag8b", batch=4), [0, 3], 2, {1}),
+    # longer ragged queries: two live Q tiles per CTA, a partial second tile, documents of 1..1000
+    "two_q_tiles": (lambda: make_custom([200, 37, 1000, 15, 1], [[0, 1, 2], [3, 4, 0], [2]], 8, 2, 128,
+                                        PosCfg("rope", 5e5, 128), [70, 33, 100], 2, seed=77), [0, 1, 2], 2, {1}),
+    "prefill70b": (lambda: make_workload("prefill70b", batch=2), [0, 1], 0, set()),
+    # MQA: prefill and the tensor-core decode mode (key range split over CTAs, merged)
+    "mqa_alibi": (lambda: make_workload("mqa_alibi", batch=4), [0, 2], 3, {0, 2}),
+}
+
+
+@pytest.mark.parametrize("case", sorted(POISON_CASES))
+def test_poisoned_cache_rows_never_reach_the_output(lk, case):
+    """Caches filled with NaN bits before the documents and query tokens are written: only the
+    written rows may influence the result.  The output must match the oracle and be bit-identical
+    to the same launches over zero-filled caches."""
+    import torch
+    make, reqs, n_steps, check = POISON_CASES[case]
+    got_nan, got_zero = {}, {}
+    _run_and_check(lk, make(), reqs, n_steps, check, poison=True, outputs=got_nan)
+    _run_and_check(lk, make(), reqs, n_steps, check, poison=False, outputs=got_zero)
+    for key in got_zero:
+        assert torch.equal(got_nan[key].view(torch.int16), got_zero[key].view(torch.int16)), \
+            f"{case} {key}: poisoned cache rows changed the output"
+
+
+def test_poisoned_cache_no_rotation_twin(lk):
+    """The kernels built without positional work (the Delta = 0 twin) over poisoned caches give
+    the same bits as over zero-filled ones."""
+    import torch
+    outs = []
+    for poison in (True, False):
+        w = make_workload("rag8b", batch=4)
+        pb = _batch(w, poison=poison, pos_kind="none")
+        pb.fill_documents()
+        o_p = pb.prefill(pb.upload_prefill())
+        o_d = pb.decode_step(pb.upload_decode(0))
+        torch.cuda.synchronize()
+        _status_clean(lk)
+        assert torch.isfinite(o_p.float()).all() and torch.isfinite(o_d.float()).all()
+        outs.append((o_p.view(torch.int16).clone(), o_d.view(torch.int16).clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_poisoned_cache_cold_document_encode(lk):
+    """Cold encode of a 130-token document (last page 2 rows) into pages full of NaN bits."""
+    import torch
+    from position_agnostic_kv_gb300.runner import bits_to_tensor, encode_document
+    L, Hq, Hkv, D = 130, 32, 1, 128
+    rng = np.random.default_rng([L, D, Hq, 1])
+    bf = lambda *shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    q, k, v = bf(L, Hq, D), bf(L, Hkv, D), bf(L, Hkv, D)
+    pages = rng.permutation(20)[:9].astype(np.int32)
+    dev = torch.device("cuda")
+    kc = torch.full((20, Hkv, 16, D), 0, dtype=torch.int16, device=dev).fill_(NAN_BITS).view(torch.bfloat16)
+    vc = kc.clone()
+    cfg = lk.pos_cfg_from("rope", D, rope_theta=1e4)
+    out = encode_document(bits_to_tensor(q, dev), bits_to_tensor(k, dev), bits_to_tensor(v, dev), pages, kc, vc, cfg)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    ref, _ = lo.materialized_attention([(lo.bf16_bits_to_f64(k), lo.bf16_bits_to_f64(v))], lo.bf16_bits_to_f64(q),
+                                       np.arange(L), PosCfg("rope", 1e4, D).as_dict())
+    assert_close(out, ref, "cold document over poisoned pages")
 
 
 def test_no_rotation_twin(lk):

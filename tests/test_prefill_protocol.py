@@ -2,10 +2,11 @@
 
 tests/prefill_protocol_model.py replays the waits, arrivals and commits of prefill_tc_kernel's
 roles under random interleavings of the roles, the TMA copies and the in-order tensor pipe.
-The protocol as built must never deadlock, alias a barrier phase, or reuse a metadata slot, a
-K/V stage or an S/P buffer too early; and the model must catch each planted protocol mistake
-(too few metadata slots, a V stage refilled without waiting for its PV, a softmax waiting on the
-wrong phase), so that a pass means something.
+The protocol as built must never deadlock, wait ahead of a barrier, alias a barrier phase, or
+reuse a metadata slot, a K/V stage or an S/P buffer too early; and the model must catch each
+planted protocol mistake (too few metadata slots, a V stage refilled without waiting for its PV,
+a softmax waiting on the wrong phase, and the earlier V-cleaning handshake whose rotation role
+skipped the V_FULL phases of tiles it did not clean), so that a pass means something.
 """
 import random
 
@@ -32,7 +33,7 @@ def test_protocol_as_built_is_safe_under_random_interleavings(part):
         try:
             pm.Sim(n, nq, CLEAN[clean], seed=seed).run()
         except pm.ProtocolError as e:
-            pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles, clean={clean}: {e}")
+            pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles: {e}")
 
 
 def _caught(make, n_runs=200):
@@ -57,14 +58,14 @@ def test_model_catches_v_stage_refilled_before_its_pv():
                 if j >= 2:
                     yield ("wait", self.K_FREE[s], j // 2 - 1)
                 self.publish(j)
-                self.K_FULL[s].arrive(self, expect_tx=1)
+                self.K_FULL[s].arrive(expect_tx=1)
                 self.issue_tma("K", j, self.K_FULL[s])
                 yield ("step",)
 
             def issue_v(j):  # planted mistake: no wait for V_FREE
                 s = j % 2
                 self.read_slot(j, "issue_v")
-                self.V_FULL[s].arrive(self, expect_tx=1)
+                self.V_FULL[s].arrive(expect_tx=1)
                 self.issue_tma("V", j, self.V_FULL[s])
                 yield ("step",)
 
@@ -80,7 +81,7 @@ def test_model_catches_v_stage_refilled_before_its_pv():
 def test_model_catches_softmax_waiting_on_the_wrong_phase():
     class EarlySoftmax(pm.Sim):
         def softmax(self, i):
-            self.Q_READY.arrive(self)
+            self.Q_READY.arrive()
             if i >= self.nq:
                 return
             yield ("step",)
@@ -95,7 +96,85 @@ def test_model_catches_softmax_waiting_on_the_wrong_phase():
                 if self.nq == 1 and j > 0:
                     yield ("wait", self.PV_DONE, j - 1)
                 self.s_buf[buf] = ("P", j)
-                self.P_FULL[buf].arrive(self)
+                self.P_FULL[buf].arrive()
             yield ("wait", self.FINAL, 0)
 
     assert _caught(lambda n, nq, clean, seed: EarlySoftmax(n, nq, CLEAN[clean], seed=seed)) > 0
+
+
+class OldVClean(pm.Sim):
+    """The earlier protocol, kept as a planted mistake.  The rotation role also zeroed the V
+    rows of a tile that held no key, waiting V_FULL only for such tiles and then arriving on a
+    V_READY barrier; the MMA thread waited V_READY (counting such tiles per stage) after V_FULL.
+    Skipping the V_FULL phases of tiles it did not clean leaves the rotation role one phase
+    AHEAD of the barrier when a clean tile follows an unclean one on the same stage whose V has
+    not landed yet; a parity wait then passes at once and the role zeroes a stage that the
+    earlier copy is still filling."""
+
+    every_phase = False
+
+    def __init__(self, *a, **kw):
+        super().__init__(*a, **kw)
+        self.V_READY = [pm.Bar(f"V_READY{s}", 1) for s in range(2)]
+        self.cleaned = [0, 0]
+
+    def v_users(self, j):
+        return super().v_users(j) | ({"clean"} if self.clean_of(j) else set())
+
+    def rotation(self):
+        for j in range(self.n):
+            s = j % 2
+            yield ("wait", self.K_FULL[s], j // 2)
+            self.read_slot(j, "rotation")
+            yield ("step",)
+            self.kstage_users[s].discard("rot")
+            self.K_READY[s].arrive()
+            if self.clean_of(j) or self.every_phase:
+                yield ("wait", self.V_FULL[s], j // 2)
+                if self.vstage[s] != j:
+                    raise pm.ProtocolError(f"V clean of tile {j} finds stage holding {self.vstage[s]}")
+                if self.clean_of(j):
+                    yield ("step",)
+                    self.vstage_users[s].discard("clean")
+                    self.V_READY[s].arrive()
+
+    def mma_wait_v(self, jj):
+        s = jj % 2
+        yield ("wait", self.V_FULL[s], jj // 2)
+        if self.clean_of(jj):
+            yield ("wait", self.V_READY[s], self.cleaned[s])
+            self.cleaned[s] += 1
+
+
+class OldVCleanEveryPhase(OldVClean):
+    """The same cleaning role, corrected: it consumes every V_FULL phase in tile order."""
+    every_phase = True
+
+
+def test_model_catches_the_old_v_clean_handshake():
+    caught = []
+    for seed, n, nq, clean in _schedules(400):
+        try:
+            OldVClean(n, nq, CLEAN[clean], seed=seed).run()
+        except pm.ProtocolError as e:
+            caught.append(str(e))
+    assert caught, "the model let the old V-clean handshake through"
+    assert any("waiter ahead" in c and "V_FULL" in c for c in caught), caught[:3]
+
+
+def test_v_clean_consuming_every_phase_is_safe():
+    """Control for the test above: the model does not reject a V-cleaning role as such."""
+    for seed, n, nq, clean in _schedules(400):
+        try:
+            OldVCleanEveryPhase(n, nq, CLEAN[clean], seed=seed).run()
+        except pm.ProtocolError as e:
+            pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles, clean={clean}: {e}")
+
+
+def test_model_flags_a_waiter_ahead_of_its_barrier():
+    """Unit check of the parity rule: a wait registered for a phase the barrier has not begun."""
+    class Ahead(pm.Sim):
+        def rotation(self):
+            yield ("wait", self.K_FULL[0], 1)  # phase 1 before phase 0 completed
+    with pytest.raises(pm.ProtocolError, match="waiter ahead"):
+        Ahead(4, 1, seed=0).run()

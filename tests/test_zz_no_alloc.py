@@ -8,8 +8,11 @@ scratch is a fixed 16 MiB array compiled into the library.
 
 This test calls that entry point through the C ABI and checks it against lazy_attn_decode
 (with a caller workspace) on the same inputs, on two calls in a row: the second call reuses
-the array the first one left behind.  It lives in a file of its own, collected last, so that a
-run stopping at the first failure has run every other test first; it needs nothing from them.
+the array the first one left behind.  Both calls run the same kernels on the same inputs, so
+their outputs must be bit-identical.  Two head groupings: 4 heads per KV head (the CUDA-core
+decode and its split merge) and 32 (MQA: the tensor-core decode, its key range split over CTAs
+and merged).  It lives in a file of its own, collected last, so that a run stopping at the
+first failure has run every other test first; it needs nothing from them.
 """
 import ctypes
 
@@ -22,12 +25,13 @@ from workloads import make_workload
 pytestmark = pytest.mark.gpu
 
 
-def test_noalloc_decode_matches_workspace_decode_on_two_calls():
+@pytest.mark.parametrize("name,batch", [("rag8b", 16), ("mqa_alibi", 4)])
+def test_noalloc_decode_matches_workspace_decode_on_two_calls(name, batch):
     import torch
     lk = lib()
     from position_agnostic_kv_gb300.runner import PagedBatch
 
-    w = make_workload("rag8b")  # 16 requests x ~2 000 keys: the decode splits its KV sequence
+    w = make_workload(name, batch=batch)  # every request over ~2 000 or ~12 000 keys
     pb = PagedBatch(w, device="cuda")
     need = lk.workspace_size(lk.PHASE_DECODE, w.B, w.B, pb.max_blocks, w.Hq, w.Hkv, w.D)
     assert need > 0, "this batch must use split scratch for the test to mean anything"
@@ -51,4 +55,6 @@ def test_noalloc_decode_matches_workspace_decode_on_two_calls():
         assert rc == 0, lk.lib.lazy_last_error()
         torch.cuda.synchronize()
         assert lk.device_status() == 0
-        assert_close(got, ref.float().cpu().numpy().astype(np.float64), f"no-alloc decode call {t + 1}")
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), \
+            f"{name}: no-alloc decode call {t + 1} differs from the workspace decode"
+        assert_close(got, ref.float().cpu().numpy().astype(np.float64), f"{name} no-alloc decode call {t + 1}")
