@@ -7,11 +7,14 @@ by their document offset), then every decode step (write the new token, attend w
 at document boundaries).  The documents were written into the cache once beforehand: that is
 the premise of the method (one cached copy per document, reused at any offset).
 
-Default workload: Llama-3.1-8B attention shape (32/8/128, RoPE theta 5e5), 16 requests x 10
-docs x 200 tokens drawn from a 200-doc pool by Zipf alpha 1.1 and shuffled, 32-token query
-prefill, then 64 decode steps, 16-token pages.  ``--sharing private`` (default) gives every
-(request, doc) its own pages so that logical bytes equal the bytes that must come from HBM;
-``shared`` keeps one physical copy per document.  Inputs are seeded synthetic bf16 N(0,1).
+Default workload (the decode-bound configuration, the largest that fits one GPU): the 8B
+attention shape (32/8/128, RoPE theta 5e5), 64 requests x 20 documents x 1600 tokens drawn from
+a 500-document pool by Zipf alpha 2.1 in random order (32 000-token contexts), 128 decode steps,
+16-token pages.  ``--sharing private`` (default) gives every (request, doc) its own pages so that
+logical bytes equal the bytes that must come from HBM; ``shared`` keeps one physical copy per
+document.  Inputs are seeded synthetic bf16 N(0,1).  The same JSON line carries the tensor-core
+prefill timed on its own on the 70B shape (``--prefill-workload``, a dense contraction) with its
+deferred-rotation overhead, and the small-batch RAG workload (``--extra``) as a sub-object.
 
 Each step is captured once as a CUDA graph and replayed; L2 is flushed (512 MB write) between
 timed steps, outside the step's own events.  Per-launch decode durations come from event
@@ -58,10 +61,14 @@ WORKLOAD_TEXT = {
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="rag8b")
+    p.add_argument("--workload", default="decode32k")
+    p.add_argument("--prefill-workload", default="prefill70b",
+                   help="workload of the separately timed tensor-core prefill ('none' to skip)")
+    p.add_argument("--extra", default="rag8b", help="comma-separated workloads also timed (sub-objects)")
+    p.add_argument("--overhead-reps", type=int, default=20, help="timed launches per overhead variant")
     p.add_argument("--sharing", choices=["private", "shared"], default="private")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -186,30 +193,35 @@ def job_throughput(dist, tokens_per_step: int, step_ms: list) -> tuple:
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, dist):
+def _prepare(w, dev, pos_kind=None):
+    """Resident batch of workload `w`: documents written once (the method's premise), the
+    step's inputs packed into one device buffer and its outputs into another, so that an
+    end-to-end run moves them with one host->device and one device->host copy per step."""
+    import torch
+    from position_agnostic_kv_gb300.runner import PagedBatch
+    pb = PagedBatch(w, device=dev, pos_kind=pos_kind)
+    pb.fill_documents()
+    torch.cuda.synchronize()
+    in_blob, (pre, *decs) = pack_views([pb.upload_prefill() if pb.total_q else {}] +
+                                       [pb.upload_decode(t) for t in range(w.n_decode)], dev)
+    out_blob, outs = pack_views([{"o": torch.empty((max(pb.total_q, 1), w.Hq, w.D), dtype=torch.bfloat16)}] +
+                                [{"o": torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16)}
+                                 for _ in range(w.n_decode)], dev)
+    return pb, (pre or None), decs, in_blob, out_blob, outs[0]["o"], [o["o"] for o in outs[1:]]
+
+
+def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=False, overhead=True):
+    """Time `steps` steps of workload `name` (each: the query tokens' KV write and prefill, then
+    every decode step's KV write and decode), captured once as a CUDA graph and replayed, L2
+    flushed before every timed step.  Returns the per-workload part of the JSON line."""
     import numpy as np
     import torch
-
-    import position_agnostic_kv_gb300 as lk
-    from position_agnostic_kv_gb300.runner import PagedBatch
     from workloads import make_workload
 
     dev = torch.device("cuda", dist.local_rank)
-    torch.cuda.set_device(dev)
-    w = make_workload(args.workload, sharing=args.sharing)
-    pb = PagedBatch(w, device=dev, pos_kind=args.pos)
-    pb.fill_documents()
-    torch.cuda.synchronize()
+    w = make_workload(name, sharing=sharing)
+    pb, pre, decs, in_blob, out_blob, out_p, outs_d = _prepare(w, dev, args.pos)
     n_dec = w.n_decode
-    # Every step's inputs live in one device buffer and its outputs in another, so that the
-    # end-to-end run moves them with one host->device and one device->host copy per step.
-    in_blob, (pre, *decs) = pack_views([pb.upload_prefill() if pb.total_q else {}] +
-                                       [pb.upload_decode(t) for t in range(n_dec)], dev)
-    pre = pre or None
-    out_blob, outs = pack_views([{"o": torch.empty((max(pb.total_q, 1), w.Hq, w.D), dtype=torch.bfloat16)}] +
-                                [{"o": torch.empty((w.B, w.Hq, w.D), dtype=torch.bfloat16)}
-                                 for _ in range(n_dec)], dev)
-    out_p, outs_d = outs[0]["o"], [o["o"] for o in outs[1:]]
     stream = torch.cuda.Stream(device=dev)
     use_graph = not args.no_graph
 
@@ -219,8 +231,7 @@ def run_ours(args, dist):
 
     # Event pairs on the prefill and on every 8th decode launch: enough samples for the
     # per-launch times, few enough event nodes to leave the step's own time unchanged.
-    ev_every = 8
-    ev_steps = list(range(0, n_dec, ev_every))
+    ev_steps = list(range(0, n_dec, 8))
     ev_pre = (mk(), mk())
     ev_dec = {t: (mk(), mk()) for t in ev_steps}
     launches = 0
@@ -269,20 +280,20 @@ def run_ours(args, dist):
             else:
                 step()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         run_step()
     torch.cuda.synchronize()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     dec_ms, pre_ms, step_ms = [], [], []
-    clocks = Clocks(dist.local_rank)
     dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    if clocks:
+        clocks.start()
     wall0 = time.perf_counter()
     inner_ok = True
-    for k in range(args.steps):
+    for k in range(steps):
         with torch.cuda.stream(stream):
             flush.zero_()
             e0[k].record(stream)
@@ -302,9 +313,9 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
     if not inner_ok:  # per-launch times from eager launches of the same step, L2 flushed
-        for _ in range(min(args.steps, 10)):
+        for _ in range(min(steps, 10)):
             with torch.cuda.stream(stream):
                 flush.zero_()
                 step()
@@ -331,59 +342,149 @@ def run_ours(args, dist):
     peaks, peak_kind = load_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
     achieved_gbs = avg_dec_bytes / (avg_dec_ms / 1e3) / 1e9 if dec_ms else None
-    pre_flops = 0
-    if pb.total_q:
-        for b in range(w.B):
-            L = int(w.q_len[b])
-            pre_flops += 4 * w.D * w.Hq * sum(int(pb.q_start_h[b]) + i + 1 for i in range(L))
+    pre_flops = prefill_flops(w, pb)
     pre_med = statistics.median(pre_ms) if pre_ms else None
     pre_tflops = pre_flops / (pre_med / 1e3) / 1e12 if pre_med else None
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     dec_total = avg_dec_ms * n_dec if dec_ms else 0.0
-    pre_total = pre_med or 0.0
-    if dec_total >= pre_total:  # the dominant kernel of the step
-        traffic = profiled_traffic("decode.cu", f"decode_{args.workload}_{args.sharing}.md")
+    if dec_total >= (pre_med or 0.0):  # the dominant kernel of the step
+        traffic = profiled_traffic("decode.cu", f"decode_{name}_{sharing}.md")
         roofline = {"kernel": "lazy_attn_decode (split-KV decode + lse merge)", "bound": "hbm",
                     "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved_gbs / hbm_peak, "peak_source": f"{peak_kind} hbm_gbs",
                     "traffic": traffic, "algorithmic_bytes_per_launch": avg_dec_bytes,
                     "avg_launch_us": avg_dec_ms * 1e3}
     else:
-        traffic = profiled_traffic("prefill_tc.cu", f"prefill_{args.workload}_{args.sharing}.md")
+        traffic = profiled_traffic("prefill_tc.cu", f"prefill_{name}_{sharing}.md")
         roofline = {"kernel": "lazy_attn_prefill (tcgen05)", "bound": "tensor", "achieved": pre_tflops,
                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": pre_tflops / bf16_peak,
                     "peak_source": f"{peak_kind} bf16_tflops (burst)", "traffic": traffic,
                     "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_med * 1e3}
     res = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) bf16; Zipf-drawn documents)",
-        "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
-                   "sharing": args.sharing, "pos": args.pos or w.pos.kind,
-                   "global_batch": w.B * dist.world, "seq_len": int(keys0.max()) + n_dec,
-                   "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{dist.world}",
-                   "l2": "flushed between timed steps (512 MB write, outside the step events)",
-                   "launch": "CUDA graph per step" if graph is not None else "eager"},
+        "value": value, "ms_per_step": mean_ms, "tokens_per_step": tokens_per_step,
+        "workload": f"{name}: {WORKLOAD_TEXT[name]}", "sharing": sharing, "pos": args.pos or w.pos.kind,
+        "global_batch": w.B * dist.world, "seq_len": int(keys0.max()) + n_dec,
+        "launch": "CUDA graph per step" if graph is not None else "eager",
         "roofline": roofline,
-        "decode": {"kernel": "lazy_attn_decode", "bytes_per_launch": avg_dec_bytes if dec_ms else None,
-                   "avg_launch_us": avg_dec_ms * 1e3 if dec_ms else None, "gbs": achieved_gbs,
-                   "timed_launches": f"decode steps {ev_steps} of every timed step (CUDA events in the graph)",
-                   "frac_hbm_peak": achieved_gbs / hbm_peak if achieved_gbs else None,
-                   "launches_per_step": n_dec},
-        "prefill": {"kernel": "lazy_attn_prefill", "flops_per_launch": pre_flops,
-                    "median_us": pre_med * 1e3 if pre_med else None, "tflops": pre_tflops,
-                    "frac_bf16_peak": pre_tflops / bf16_peak if pre_tflops else None,
-                    "peak_source": f"{peak_kind} bf16_tflops"},
-        "gpu_launches": launches * args.steps,
-        "clocks": clk,
+        "decode": None if not n_dec else {
+            "kernel": "lazy_attn_decode", "bytes_per_launch": avg_dec_bytes if dec_ms else None,
+            "avg_launch_us": avg_dec_ms * 1e3 if dec_ms else None, "gbs": achieved_gbs,
+            "timed_launches": f"decode steps {ev_steps} of every timed step (CUDA events in the graph)",
+            "frac_hbm_peak": achieved_gbs / hbm_peak if achieved_gbs else None,
+            "launches_per_step": n_dec},
+        "step_prefill": None if pre is None else {
+            "kernel": "lazy_attn_prefill", "flops_per_launch": pre_flops,
+            "median_us": pre_med * 1e3 if pre_med else None, "tflops": pre_tflops,
+            "frac_bf16_peak": pre_tflops / bf16_peak if pre_tflops else None,
+            "hbm_bytes_per_launch": prefill_bytes(w, pb),
+            "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "gpu_launches": launches * steps,
         "wall_s_timed_region": wall,
     }
-    if not args.no_overhead and pb.cfg.kind in (lk.POS_ROPE, lk.POS_YARN):
+    if clk is not None:
+        res["clocks"] = clk
+    if overhead and pb.cfg.kind in (lk.POS_ROPE, lk.POS_YARN):
         res["rotation_overhead"] = rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush)
-    if not args.no_e2e:
+    if e2e:
         res["e2e"] = run_e2e(args, in_blob, out_blob, run_step, stream, dist, tokens_per_step)
+    del graph
+    return res
+
+
+def prefill_flops(w, pb) -> int:
+    """4 D Hq x (keys visible to each query row), summed: QK^T and PV, causal-exact."""
+    flops = 0
+    for b in range(w.B):
+        L = int(w.q_len[b])
+        flops += 4 * w.D * w.Hq * sum(int(pb.q_start_h[b]) + i + 1 for i in range(L))
+    return flops
+
+
+def prefill_bytes(w, pb) -> int:
+    """Unique bytes a prefill launch must move: every visible key's K and V row once per KV head
+    (Q rows and outputs included)."""
+    keys = sum(int(pb.q_start_h[b]) + int(w.q_len[b]) for b in range(w.B) if w.q_len[b])
+    return keys * w.Hkv * w.D * 2 * 2 + 2 * pb.total_q * w.Hq * w.D * 2
+
+
+def prefill_probe(args, dist, lk, name, sharing):
+    """The tensor-core prefill on its own workload (by default the 70B shape, whose prefill is
+    a dense contraction): median of eager launches with L2 flushed before each, over the same
+    resident caches as its Delta = 0 twin (the rotation_overhead runs)."""
+    import torch
+    from workloads import make_workload
+    dev = torch.device("cuda", dist.local_rank)
+    w = make_workload(name, sharing=sharing)
+    pb, pre, _, _, _, out_p, _ = _prepare(w, dev, None)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        lk.kv_write(pre["k"], pre["v"], pre["slot"], pre["lp"], pb.k_cache, pb.v_cache, pb.cfg, stream=stream)
+    stream.synchronize()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ovh = rotation_overhead(args, lk, pb, pre, [], out_p, [], stream, flush)
+    peaks, peak_kind = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    flops = prefill_flops(w, pb)
+    us = ovh["prefill"]["rot_us"]
+    tflops = flops / (us / 1e6) / 1e12
+    return {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "sharing": sharing,
+            "kernel": "lazy_attn_prefill (tcgen05)", "flops_per_launch": flops,
+            "hbm_bytes_per_launch": prefill_bytes(w, pb), "median_us": us, "tflops": tflops,
+            "frac_bf16_peak": tflops / bf16_peak, "peak": bf16_peak,
+            "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed on its own)",
+            "timing": "eager launches, L2 flushed before each, median (same runs as rotation_overhead)",
+            "traffic": profiled_traffic("prefill_tc.cu", f"prefill_{name}_{sharing}.md"),
+            "rotation_overhead": ovh["prefill"] | {"method": ovh["method"],
+                                                   **({"launch_errors": ovh["launch_errors"]}
+                                                      if "launch_errors" in ovh else {})}}
+
+
+def run_ours(args, dist):
+    import torch
+    import position_agnostic_kv_gb300 as lk
+
+    torch.cuda.set_device(dist.local_rank)
+    clocks = Clocks(dist.local_rank)
+    main = measure_step(args, dist, lk, args.workload, args.sharing, args.steps, args.warmup, clocks=clocks,
+                        e2e=not args.no_e2e, overhead=not args.no_overhead)
+    res = {
+        "metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; Zipf-drawn documents)",
+        "config": {"workload": main["workload"], "sharing": main["sharing"], "pos": main["pos"],
+                   "global_batch": main["global_batch"], "seq_len": main["seq_len"],
+                   "tokens_per_step": main["tokens_per_step"], "parallelism": f"replicas x{dist.world}",
+                   "l2": "flushed between timed steps (512 MB write, outside the step events); "
+                         "the K/V read per step also exceeds L2",
+                   "launch": main["launch"]},
+        "roofline": main["roofline"],
+        "decode": main["decode"],
+        "gpu_launches": main["gpu_launches"],
+        "clocks": main.get("clocks"),
+        "wall_s_timed_region": main["wall_s_timed_region"],
+    }
+    if main["step_prefill"] is not None:
+        res["step_prefill"] = main["step_prefill"]
+    ovh = {}
+    if "rotation_overhead" in main:
+        ovh = {k: v for k, v in main["rotation_overhead"].items()}
+    if args.prefill_workload != "none":
+        res["prefill"] = prefill_probe(args, dist, lk, args.prefill_workload, args.sharing)
+        ovh["prefill_" + args.prefill_workload] = res["prefill"]["rotation_overhead"]
+    if ovh:
+        res["rotation_overhead"] = ovh
+    extra = {}
+    for name in [x for x in args.extra.split(",") if x and x != args.workload]:
+        e = measure_step(args, dist, lk, name, args.sharing, min(args.steps, 20), args.warmup,
+                         overhead=not args.no_overhead)
+        extra[name] = {k: e[k] for k in ("value", "ms_per_step", "tokens_per_step", "workload", "decode",
+                                         "step_prefill", "rotation_overhead", "roofline") if k in e}
+    if extra:
+        res["extra_workloads"] = extra
+    if "e2e" in main:
+        res["e2e"] = main["e2e"]
     return res
 
 
@@ -399,7 +500,7 @@ def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
     meta0_h = pb.meta_h & ~np.uint64(0xFFFFFF << 16)  # Delta field cleared
     meta0 = torch.from_numpy(meta0_h.view(np.int64)).to(pb.meta.device)
     variants = {"rot": (pb.cfg, pb.meta), "delta0": (cfg_none, pb.meta), "same_delta": (pb.cfg, meta0)}
-    reps = max(5, min(args.steps, 20))
+    reps = max(5, args.overhead_reps)
     dec_idx = list(range(0, len(decs), max(1, len(decs) // 8)))[:8]
     out = {}
     errors, statuses = {}, set()
@@ -543,27 +644,37 @@ def oracle_sample(w, reqs, n_dec):
     return run, tokens
 
 
+# Bounded oracle samples per workload: (requests, decode steps) for the CPU baseline of our
+# line, and for one step of the reference arm.  One decode step of one decode32k request (32 000
+# keys rotated and attended in fp64) takes about 0.6 s on 16 Arm cores.
+ORACLE_SAMPLE = {"decode32k": ((8, 2), (2, 1)), "prefill70b": ((2, 0), (1, 0))}
+DEFAULT_SAMPLE = ((8, 16), (1, 2))
+
+
 def cpu_baseline(args):
     from workloads import make_workload
     w = make_workload(args.workload, sharing=args.sharing)
-    reqs = list(range(min(w.B, 8)))
-    n_dec = min(w.n_decode, 16)
+    (n_req, n_dec), _ = ORACLE_SAMPLE.get(args.workload, DEFAULT_SAMPLE)
+    reqs = list(range(min(w.B, n_req)))
+    n_dec = min(w.n_decode, n_dec)
     run, tokens = oracle_sample(w, reqs, n_dec)
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
+    what = (f"their query prefill + {n_dec} decode steps" if w.q_len.sum() else f"{n_dec} decode step(s)")
     return {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": f"{len(reqs)} requests of {args.workload}: their query prefill + {n_dec} decode "
-                      f"steps ({tokens} tokens, {dt:.1f} s, NumPy fp64, BLAS threads = all cores)"}
+            "sample": f"{len(reqs)} requests of {args.workload}: {what} ({tokens} tokens, {dt:.1f} s, "
+                      f"NumPy fp64, BLAS threads = all cores)"}
 
 
 def run_reference(args, dist):
     """The oracle as the reference arm: each step = one bounded sample of the workload."""
     from workloads import make_workload
     w = make_workload(args.workload, sharing=args.sharing)
-    reqs = [0]
-    n_dec = min(w.n_decode, 2)
+    _, (n_req, n_dec) = ORACLE_SAMPLE.get(args.workload, DEFAULT_SAMPLE)
+    reqs = list(range(min(w.B, n_req)))
+    n_dec = min(w.n_decode, n_dec)
     run, tokens = oracle_sample(w, reqs, n_dec)
     for _ in range(args.warmup):
         run()
@@ -580,9 +691,9 @@ def run_reference(args, dist):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) bf16; Zipf-drawn documents)",
             "config": {"workload": f"{args.workload}: {WORKLOAD_TEXT[args.workload]}",
-                       "sharing": args.sharing, "sample_per_step": f"request 0: query prefill + {n_dec} decode steps"},
+                       "sharing": args.sharing, "sample_per_step": f"request 0: query prefill (if any) + {n_dec} decode steps"},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"request 0 of {args.workload}: prefill + {n_dec} decode steps ({tokens} tokens) per step"},
+                             "sample": f"request 0 of {args.workload}: prefill (if any) + {n_dec} decode steps ({tokens} tokens) per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
