@@ -55,8 +55,11 @@ constexpr int kM = 128;            // query rows per Q tile
 constexpr int kQT = 2;             // Q tiles per CTA
 constexpr int kN = 128;            // keys per K/V tile
 constexpr int kPagesPerTile = kN / kPage;
-constexpr int kStages = 2;         // K ring and V ring depth
-constexpr int kSlots = 4;          // per-tile metadata slots (tile j uses slot j % 4)
+constexpr int kKStages = 3;        // K ring depth: K runs two tiles ahead of V
+constexpr int kVStages = 2;        // V ring depth
+constexpr int kSlots = 6;          // per-tile metadata slots (tile j uses slot j % 6): with K two
+                                   // tiles ahead, tile j + 4 is published while the softmax of
+                                   // tile j may still read its slot (one live Q tile)
 constexpr int kThreads = 512;
 constexpr int kRotWarp0 = 8;
 constexpr int kProdWarp = 12;
@@ -74,17 +77,17 @@ constexpr float kTau = 8.0f;
 
 // barrier indices
 enum : int {
-  B_K_FULL = 0,    // [2] K tile landed (TMA bytes)
-  B_K_READY = 2,   // [2] K tile rotated (128 arrivals)
-  B_K_FREE = 4,    // [2] both QK^T done with the K stage (commit)
-  B_V_FULL = 6,    // [2] V tile landed (TMA bytes)
-  B_V_FREE = 8,    // [2] both PV done with the V stage (commit)
-  B_S_FULL = 10,   // [2] per Q tile (one live tile: per S buffer): S written (commit)
-  B_P_FULL = 12,   // [2] per Q tile (one live tile: per S buffer): P in TMEM, O rescaled (128)
-  B_Q_READY = 14,  // both Q tiles prepared (256 arrivals)
-  B_FINAL = 15,    // all MMAs finished (commit)
-  B_PV_DONE = 16,  // one live Q tile only: PV of a tile finished (commit)
-  NBAR = 17
+  B_K_FULL = 0,    // [3] K tile landed (TMA bytes)
+  B_K_READY = 3,   // [3] K tile rotated (128 arrivals)
+  B_K_FREE = 6,    // [3] both QK^T done with the K stage (commit)
+  B_V_FULL = 9,    // [2] V tile landed (TMA bytes)
+  B_V_FREE = 11,   // [2] both PV done with the V stage (commit)
+  B_S_FULL = 13,   // [2] per Q tile (one live tile: per S buffer): S written (commit)
+  B_P_FULL = 15,   // [2] per Q tile (one live tile: per S buffer): P in TMEM, O rescaled (128)
+  B_Q_READY = 17,  // both Q tiles prepared (256 arrivals)
+  B_FINAL = 18,    // all MMAs finished (commit)
+  B_PV_DONE = 19,  // one live Q tile only: PV of a tile finished (commit)
+  NBAR = 20
 };
 // Every waiter consumes every phase of the barriers it waits on, in order: a parity wait
 // (mbarrier.try_wait.parity) cannot tell the phase it asks for from the one two phases
@@ -98,18 +101,14 @@ struct Layout {
   static constexpr int QTILE = kM * D * 2;                 // one Q tile
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + kQT * QTILE;        // K ring
-  static constexpr int V_OFF = K_OFF + kStages * TILE;     // V ring
-  static constexpr int PSTART_OFF = V_OFF + kStages * TILE;  // int [slot][8] key position of stage row 0
-  static constexpr int RUN_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int [slot][8] first page of
-                                                                         // the page's run of equal Delta
-  static constexpr int PINFO_OFF = RUN_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, lo}:
-                                                                         // stage rows [lo, 16) hold keys
+  static constexpr int V_OFF = K_OFF + kKStages * TILE;    // V ring
+  static constexpr int PSTART_OFF = V_OFF + kVStages * TILE;  // int [slot][8] key position of stage row 0
+  static constexpr int PINFO_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, lo}:
+                                                                            // stage rows [lo, 16) hold keys
   static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, unused}
   static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] page * Hkv + head
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
-  static constexpr int CS_OFF = TURNS_OFF + (D / 2) * 8;                // float2 [2][8][D/2]
-  static constexpr int CS_BUF = kPagesPerTile * (D / 4);                 // float4 per buffer
-  static constexpr int BAR_OFF = CS_OFF + 2 * kPagesPerTile * (D / 2) * 8;
+  static constexpr int BAR_OFF = TURNS_OFF + (D / 2) * 8;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;                   // tmem slot, abort flag
   static constexpr int SMEM = MISC_OFF + 16 + 1024;                     // + alignment slack
 };
@@ -260,7 +259,7 @@ template <int D, int POS>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
   using L = Layout<D>;
-  constexpr bool kRotate = (POS == kRope || POS == kYarn);
+  constexpr bool kRotate = (POS == kRope || POS == kRopeX);
   // With rotation, the rotated Q and K are rounded once more before QK^T: write them as f16
   // (10 mantissa bits; stored bf16 keys convert exactly) so QK^T runs as an f16 x f16 MMA.
   // Without rotation K is the stored bf16 itself, so Q is rounded to bf16.  PV is bf16 x bf16.
@@ -305,21 +304,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
   const uint32_t sQ0 = sb + L::Q_OFF, sK0 = sb + L::K_OFF, sV0 = sb + L::V_OFF;
   int* pstart = reinterpret_cast<int*>(sm + L::PSTART_OFF);
-  int* prun = reinterpret_cast<int*>(sm + L::RUN_OFF);
   int2* pinfo = reinterpret_cast<int2*>(sm + L::PINFO_OFF);
   int* flags = reinterpret_cast<int*>(sm + L::FLAG_OFF);
   unsigned long long* turns = reinterpret_cast<unsigned long long*>(sm + L::TURNS_OFF);
-  float4* cs4 = reinterpret_cast<float4*>(sm + L::CS_OFF);
   const uint32_t bar0 = sb + L::BAR_OFF;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::MISC_OFF + 4);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(BAR(B_K_FULL + s), 1);
       mbar_init(BAR(B_K_READY + s), 128);
       mbar_init(BAR(B_K_FREE + s), 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(BAR(B_V_FULL + s), 1);
       mbar_init(BAR(B_V_FREE + s), 1);
     }
@@ -570,56 +569,65 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
   } else if (warp < kProdWarp) {
     // ============================ K rotation
+    // Thread rt works on page slot ps = rt / 16 of every tile.  Full half-split rotation: it owns
+    // chunk pair c (dims 8c..8c+7 and their partners 8c+D/2..) for NCP rows of the page and keeps
+    // the cos/sin of those 8 frequencies in registers, recomputed only when its page slot's
+    // Delta changes (pages inside one document share it), so there is no cos/sin buffer and no
+    // barrier among the rotation threads.  Partial rotary_dim / interleaved pairs: each thread
+    // owns one chunk task (a rotated chunk pair or chunk, or one unrotated chunk converted to
+    // f16) for all 16 rows of its page.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::rot));
     const int rt = threadIdx.x - kRotWarp0 * 32;
-    const int ps = rt / kPage, t = rt % kPage;  // this thread's page slot and row in every tile
-    bool ok = true;  // once a wait gives up, the thread skips work but keeps every named barrier
-    // A tile whose pages are one run of the same Delta as the previous tile's single run (the
-    // middle of a long document) reuses that tile's cos/sin buffer; otherwise the rows go to the
-    // other buffer, which no thread still reads once all passed the previous tile's barrier.
-    int cs_buf = 1, cs_delta = -1;  // buffer and Delta of the last single-run tile (-1: none)
+    const int ps = rt / kPage, l = rt % kPage;
+    constexpr int NCP = D / 16;  // chunk pairs per row (full width)
+    bool ok = true;              // once a wait gives up, the thread skips work but keeps arriving
+    float co[8], sn[8];
+    int cur_delta = -1;
+    // this thread's task in the generic layout: rotated chunk pair / chunk (kind 0 / 1) or tail
+    // chunk converted to f16 (kind 2), or nothing (kind 3)
+    int g_kind = 3, g_chunk = 0, g_part = 0, g_f0 = 0;
+    if constexpr (POS == kRopeX) {
+      const int rd = a.pos.rotary_dim;
+      const int nrot = a.pos.interleaved ? rd / 8 : rd / 16, ntail = (D - rd) / 8;
+      if (l < nrot) {
+        g_kind = a.pos.interleaved ? 1 : 0;
+        g_chunk = l;
+        g_part = l + rd / 16;                  // half-split partner chunk
+        g_f0 = a.pos.interleaved ? 4 * l : 8 * l;  // first frequency of the task
+      } else if (l < nrot + ntail) {
+        g_kind = 2;
+        g_chunk = rd / 8 + (l - nrot);
+      }
+    }
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kStages, slot = j % kSlots;
-      const uint32_t par = uint32_t((j / kStages) & 1);
-      if (ok) ok = wait_bar(BAR(B_K_FULL + s), par, abort_flag, a.status);
-      const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, lo}
+      const int s = j % kKStages, slot = j % kSlots;
+      if (ok) ok = wait_bar(BAR(B_K_FULL + s), uint32_t((j / kKStages) & 1), abort_flag, a.status);
       if constexpr (kRotate) {
+        const int2 pi = ok ? pinfo[slot * kPagesPerTile + ps] : make_int2(0, kPage);  // {Delta, lo}
         const uint32_t sK = sK0 + uint32_t(s * L::TILE);
-        // cos/sin rows only for pages that start a new document offset: page pp uses the row of
-        // the first page of its run of equal Delta (consecutive pages of a document share it)
-        const int run_start = ok ? prun[slot * kPagesPerTile + ps] : 0;
-        const int d0 = ok ? pinfo[slot * kPagesPerTile].x : -1;
-        const bool single = ok && prun[slot * kPagesPerTile + kPagesPerTile - 1] == 0;  // same for all
-        const bool reuse = single && d0 == cs_delta;
-        if (!reuse) cs_buf ^= 1;
-        cs_delta = single ? d0 : -1;
-        for (int idx = rt; ok && !reuse && idx < kPagesPerTile * (D / 4); idx += 128) {
-          const int pp = idx / (D / 4), q = idx % (D / 4);
-          const int dl = pinfo[slot * kPagesPerTile + pp].x;
-          if (prun[slot * kPagesPerTile + pp] == pp) {
-            float s0, c0, s1, c1;
-            turn_sincos_fast(uint32_t(dl), turns[2 * q], s0, c0);
-            turn_sincos_fast(uint32_t(dl), turns[2 * q + 1], s1, c1);
-            cs4[cs_buf * L::CS_BUF + idx] = make_float4(c0, c1, s0, s1);
-          }
-        }
-        named_sync(1, 128);
-        if (ok && t >= pi.y) {  // rows before lo hold zeros (no key)
-          const float4* c4 = cs4 + cs_buf * L::CS_BUF + run_start * (D / 4);
-          const int rd = a.pos.rotary_dim;
-          if (rd == D && !a.pos.interleaved) {  // full half-split rotation (the common case)
+        if (pi.y < kPage) {  // the page holds keys (rows before lo are zeros)
+          if constexpr (POS == kRope) {
+            const int c = l % NCP, g = l / NCP;
+            if (pi.x != cur_delta) {
+              cur_delta = pi.x;
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-              // pair i = c*8 + e: element i and its partner i + D/2 share the swizzled chunk slot
-              const uint32_t a1 = sK + swz(rt, c);
-              const uint32_t a2 = (D == 128) ? sK + uint32_t(L::BLK) + swz(rt, c) : sK + swz(rt, c + 4);
+              for (int e = 0; e < 8; ++e) turn_sincos_fast(uint32_t(pi.x), turns[8 * c + e], sn[e], co[e]);
+            }
+#pragma unroll
+            for (int i = 0; i < NCP; ++i) {
+              const int t = g * NCP + i;
+              if (t < pi.y) continue;
+              const int r = ps * kPage + t;  // row of the tile
+              // element 8c + e and its partner 8c + e + D/2: the same chunk slot of the other
+              // column block (D = 128) or chunk c + 4 of the same block (D = 64)
+              const uint32_t a1 = sK + swz(r, c);
+              const uint32_t a2 = (D == 128) ? sK + uint32_t(L::BLK) + swz(r, c) : sK + swz(r, c + 4);
               uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
               uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
               uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
 #pragma unroll
               for (int w = 0; w < 4; ++w) {
-                const float4 cc = c4[c * 4 + w];  // pairs c*8 + 2w, c*8 + 2w + 1
-                const float2 cv = make_float2(cc.x, cc.y), sv = make_float2(cc.z, cc.w);
+                const float2 cv = make_float2(co[2 * w], co[2 * w + 1]), sv = make_float2(sn[2 * w], sn[2 * w + 1]);
                 const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
                 const float2 t1 = __fmul2_rn(x2, sv), t2 = __fmul2_rn(x2, cv);
                 const float2 y1 = __ffma2_rn(x1, cv, make_float2(-t1.x, -t1.y));  // x1 c - x2 s
@@ -630,50 +638,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
               st_shared_v4(a1, u1);
               st_shared_v4(a2, u2);
             }
-          } else {  // partial rotary_dim and / or interleaved pairs
-            auto kaddr = [&](int k) { return sK + uint32_t((k >> 3) * L::BLK) + swz(rt, k & 7); };
-            if (!a.pos.interleaved) {
-              const int hc = rd / 16;
+          } else {  // POS == kRopeX
+            auto kaddr = [&](int r, int k) { return sK + uint32_t((k >> 3) * L::BLK) + swz(r, k & 7); };
+            if (g_kind < 2 && pi.x != cur_delta) {
+              cur_delta = pi.x;
+              const int nf = g_kind == 0 ? 8 : 4;
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (e < nf) turn_sincos_fast(uint32_t(pi.x), turns[g_f0 + e], sn[e], co[e]);
+            }
 #pragma unroll 1
-              for (int c = 0; c < hc; ++c) {  // chunk c against its partner c + rotary_dim/16
-                const uint32_t a1 = kaddr(c), a2 = kaddr(c + hc);
+            for (int t = pi.y; t < kPage && g_kind < 3; ++t) {
+              const int r = ps * kPage + t;
+              if (g_kind == 0) {  // half-split pairs: chunk against its partner chunk + rotary_dim/16
+                const uint32_t a1 = kaddr(r, g_chunk), a2 = kaddr(r, g_part);
                 uint4 u1 = ld_shared_v4(a1), u2 = ld_shared_v4(a2);
                 uint32_t* p1 = reinterpret_cast<uint32_t*>(&u1);
                 uint32_t* p2 = reinterpret_cast<uint32_t*>(&u2);
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                  const float4 cc = c4[c * 4 + w];
                   const float2 x1 = bf2_to_f2(p1[w]), x2 = bf2_to_f2(p2[w]);
-                  p1[w] = f2_to_h2(x1.x * cc.x - x2.x * cc.z, x1.y * cc.y - x2.y * cc.w);
-                  p2[w] = f2_to_h2(x1.x * cc.z + x2.x * cc.x, x1.y * cc.w + x2.y * cc.y);
+                  p1[w] = f2_to_h2(x1.x * co[2 * w] - x2.x * sn[2 * w], x1.y * co[2 * w + 1] - x2.y * sn[2 * w + 1]);
+                  p2[w] = f2_to_h2(x1.x * sn[2 * w] + x2.x * co[2 * w], x1.y * sn[2 * w + 1] + x2.y * co[2 * w + 1]);
                 }
                 st_shared_v4(a1, u1);
                 st_shared_v4(a2, u2);
-              }
-            } else {
-#pragma unroll 1
-              for (int k = 0; k < rd / 8; ++k) {  // word w = (x_2i, x_2i+1), pair i = 4k + w
-                const uint32_t a1 = kaddr(k);
+              } else if (g_kind == 1) {  // adjacent pairs (x_2i, x_2i+1), i = 4 chunk + w
+                const uint32_t a1 = kaddr(r, g_chunk);
                 uint4 u = ld_shared_v4(a1);
                 uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                  const float4 cc = c4[2 * k + (w >> 1)];  // frequencies 2q, 2q+1 with q = i / 2
-                  const float co = (w & 1) ? cc.y : cc.x, sn = (w & 1) ? cc.w : cc.z;
                   const float x0 = bf_lo(pw[w]), x1 = bf_hi(pw[w]);
-                  pw[w] = f2_to_h2(x0 * co - x1 * sn, x0 * sn + x1 * co);
+                  pw[w] = f2_to_h2(x0 * co[w] - x1 * sn[w], x0 * sn[w] + x1 * co[w]);
                 }
                 st_shared_v4(a1, u);
-              }
-            }
-#pragma unroll 1
-            for (int k = rd / 8; k < D / 8; ++k) {  // unrotated tail: bf16 -> f16 (one MMA type)
-              const uint32_t a1 = kaddr(k);
-              uint4 u = ld_shared_v4(a1);
-              uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
+              } else {  // unrotated tail: bf16 -> f16 (QK^T has one operand type)
+                const uint32_t a1 = kaddr(r, g_chunk);
+                uint4 u = ld_shared_v4(a1);
+                uint32_t* pw = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
-              for (int w = 0; w < 4; ++w) pw[w] = f2_to_h2(bf_lo(pw[w]), bf_hi(pw[w]));
-              st_shared_v4(a1, u);
+                for (int w = 0; w < 4; ++w) pw[w] = f2_to_h2(bf_lo(pw[w]), bf_hi(pw[w]));
+                st_shared_v4(a1, u);
+              }
             }
           }
         }
@@ -702,7 +709,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       int issued_k = 0, issued_v = 0;
       // K of tile j: wait for its stage, publish the tile's metadata, load the pages
       auto issue_k = [&](int j) -> bool {
-        const int s = j % kStages, slot = j % kSlots;
+        const int s = j % kKStages, slot = j % kSlots;
         const uint64_t w = w_next;
         w_next = fetch(j + 1);  // prefetch: its latency overlaps this tile's waits
         // rows: keys of the page that some row of this CTA may see.  Only a document's last page
@@ -721,19 +728,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           }
         }
         const int lo = kPage - rows;  // the page is loaded from row -lo: stage rows [lo, 16) hold its keys
-        if (j >= kStages) {
-          const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+        if (j >= kKStages) {
+          const bool freed = wait_bar(BAR(B_K_FREE + s), uint32_t(((j / kKStages) - 1) & 1), abort_flag, a.status);
           if (!__all_sync(0xffffffffu, freed)) return false;
         }
-        const int prev_delta = __shfl_up_sync(0xffffffffu, delta, 1);
-        const uint32_t runs = __ballot_sync(0xffffffffu, lane >= 1 && lane < kPagesPerTile && delta != prev_delta);
         const int zc = page * a.Hkv + g;  // page-head coordinate of the tensor map
         if (lane < kPagesPerTile) {
           pinfo[slot * kPagesPerTile + lane] = make_int2(delta, lo);
           pgid[slot * kPagesPerTile + lane] = rows > 0 ? zc : -1;
           pstart[slot * kPagesPerTile + lane] = start - lo;
-          const uint32_t upto = runs & ((2u << lane) - 1u);  // run starts at or before this page
-          prun[slot * kPagesPerTile + lane] = upto ? 31 - __clz(upto) : 0;
         }
         const int all16 = __all_sync(0xffffffffu, lane >= kPagesPerTile || rows == kPage);
         const int last_start = __shfl_sync(0xffffffffu, start, kPagesPerTile - 1);
@@ -756,9 +759,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       // block gets no load; its stage rows still meet the PV MMA (with zero weights), so they are
       // cleared here, after the stage's previous PV is done, instead of keeping stale bits.
       auto issue_v = [&](int j) -> bool {
-        const int s = j % kStages, slot = j % kSlots;
-        if (j >= kStages) {
-          const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kStages) - 1) & 1), abort_flag, a.status);
+        const int s = j % kVStages, slot = j % kSlots;
+        if (j >= kVStages) {
+          const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kVStages) - 1) & 1), abort_flag, a.status);
           if (!__all_sync(0xffffffffu, freed)) return false;
         }
         const uint32_t sV = sV0 + uint32_t(s * L::TILE);
@@ -790,21 +793,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         issued_v = j + 1;
         return true;
       };
-      bool ok = issue_k(0);
+      // K runs kKStages - 1 tiles ahead of V: K0 K1 K2 V0 K3 V1 ...
+      bool ok = true;
+      for (int j = 0; j < kKStages - 1 && j < ntiles && ok; ++j) ok = issue_k(j);
       for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles) ok = issue_k(j + 1);
+        if (j + kKStages - 1 < ntiles) ok = issue_k(j + kKStages - 1);
         if (ok) ok = issue_v(j);
       }
       // never leave copies in flight: wait (bounded) for the last loads of every stage
       if (lane == 0) {
-        for (int j = max(0, issued_k - kStages); j < issued_k; ++j) {
-          const uint32_t bar = BAR(B_K_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+        for (int j = max(0, issued_k - kKStages); j < issued_k; ++j) {
+          const uint32_t bar = BAR(B_K_FULL + j % kKStages), par = uint32_t((j / kKStages) & 1);
           WaitClock clk;
           while (!mbar_test(bar, par) && !clk.expired()) {
           }
         }
-        for (int j = max(0, issued_v - kStages); j < issued_v; ++j) {
-          const uint32_t bar = BAR(B_V_FULL + j % kStages), par = uint32_t((j / kStages) & 1);
+        for (int j = max(0, issued_v - kVStages); j < issued_v; ++j) {
+          const uint32_t bar = BAR(B_V_FULL + j % kVStages), par = uint32_t((j / kVStages) & 1);
           WaitClock clk;
           while (!mbar_test(bar, par) && !clk.expired()) {
           }
@@ -817,7 +822,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         constexpr uint32_t IPV = idesc_mma(kM, D, 1, 0);
         bool ok = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
         auto qk = [&](int qt, int j) {  // S_qt = Q_qt K_j^T
-          const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE), sQ = sQ0 + uint32_t(qt * L::QTILE);
+          const uint32_t sK = sK0 + uint32_t((j % kKStages) * L::TILE), sQ = sQ0 + uint32_t(qt * L::QTILE);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
@@ -827,22 +832,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           mma_commit(BAR(B_S_FULL + qt));
         };
         auto pv = [&](int qt, int jj) {  // O_qt += P_qt V_jj, P from TMEM (8 columns per 16 keys)
-          const uint32_t sV = sV0 + uint32_t((jj % kStages) * L::TILE);
+          const uint32_t sV = sV0 + uint32_t((jj % kVStages) * L::TILE);
 #pragma unroll
           for (int kk = 0; kk < kN / 16; ++kk)
             mma_ts(tmem + uint32_t(2 * kN + qt * 128), tmem + uint32_t(qt * kN + kk * 8),
                    sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (jj > 0 || kk > 0) ? 1u : 0u);
         };
         auto wait_v = [&](int jj) -> bool {  // every V_FULL phase of both stages, in tile order
-          return wait_bar(BAR(B_V_FULL + jj % kStages), uint32_t((jj / kStages) & 1), abort_flag, a.status);
+          return wait_bar(BAR(B_V_FULL + jj % kVStages), uint32_t((jj / kVStages) & 1), abort_flag, a.status);
         };
         if (nq == 1) {
           // one live Q tile: tile j's scores in S_{j%2}; order QK(0) QK(1) | PV(0) QK(2) | PV(1) ...
           auto qk1 = [&](int j) -> bool {
-            if (!wait_bar(BAR(B_K_READY + j % kStages), uint32_t((j / kStages) & 1), abort_flag, a.status))
+            if (!wait_bar(BAR(B_K_READY + j % kKStages), uint32_t((j / kKStages) & 1), abort_flag, a.status))
               return false;
             tc_fence_after();
-            const uint32_t sK = sK0 + uint32_t((j % kStages) * L::TILE);
+            const uint32_t sK = sK0 + uint32_t((j % kKStages) * L::TILE);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = uint32_t((kk >> 2) * L::BLK + (kk & 3) * 32);
@@ -850,7 +855,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                        kk > 0 ? 1u : 0u);
             }
             mma_commit(BAR(B_S_FULL + (j & 1)));
-            mma_commit(BAR(B_K_FREE + j % kStages));
+            mma_commit(BAR(B_K_FREE + j % kKStages));
             return true;
           };
           if (ok) ok = qk1(0);
@@ -860,13 +865,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                  wait_v(j);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t sV = sV0 + uint32_t((j % kStages) * L::TILE);
+            const uint32_t sV = sV0 + uint32_t((j % kVStages) * L::TILE);
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk)
               mma_ts(tmem + uint32_t(2 * kN), tmem + uint32_t((j & 1) * kN + kk * 8),
                      sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(BAR(B_PV_DONE));
-            mma_commit(BAR(B_V_FREE + j % kStages));
+            mma_commit(BAR(B_V_FREE + j % kVStages));
             if (j + 2 < ntiles) ok = qk1(j + 2);
           }
           ok = false;  // the two-tile schedule below is skipped
@@ -879,14 +884,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           mma_commit(BAR(B_K_FREE));
         }
         for (int j = 1; j < ntiles && ok; ++j) {
-          const int s = j % kStages, sp = (j - 1) % kStages;
+          const int s = j % kKStages, sp = (j - 1) % kVStages;
           if (!wait_bar(BAR(B_P_FULL), uint32_t((j - 1) & 1), abort_flag, a.status) || !wait_v(j - 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           pv(0, j - 1);
-          if (!wait_bar(BAR(B_K_READY + s), uint32_t((j / kStages) & 1), abort_flag, a.status)) {
+          if (!wait_bar(BAR(B_K_READY + s), uint32_t((j / kKStages) & 1), abort_flag, a.status)) {
             ok = false;
             break;
           }
@@ -918,7 +923,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
               pv(1, jl);
             }
           }
-          if (ok) mma_commit(BAR(B_V_FREE + jl % kStages));
+          if (ok) mma_commit(BAR(B_V_FREE + jl % kVStages));
         }
         // every MMA must be complete before TMEM is released (and before the epilogue reads O)
         mma_commit(BAR(B_FINAL));
@@ -1042,13 +1047,18 @@ int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, c
   a.part_o = part_o;
   a.part_ml = part_ml;
   if (seq_len) max_q = 1;
-  const int kind = (pos.kind == kYarn) ? kRope : pos.kind;
+  // YaRN differs from RoPE only in its frequencies (already in pos.turns); partial rotary_dim or
+  // interleaved pairs take the generic rotation (kRopeX)
+  int kind = (pos.kind == kYarn) ? kRope : pos.kind;
+  if (kind == kRope && (pos.rotary_dim != D || pos.interleaved)) kind = kRopeX;
   if (D == 128) {
     if (kind == kRope) return launch_tc<128, kRope>(mk, mv, a, max_q, st);
+    if (kind == kRopeX) return launch_tc<128, kRopeX>(mk, mv, a, max_q, st);
     if (kind == kAlibi) return launch_tc<128, kAlibi>(mk, mv, a, max_q, st);
     return launch_tc<128, kNone>(mk, mv, a, max_q, st);
   }
   if (kind == kRope) return launch_tc<64, kRope>(mk, mv, a, max_q, st);
+  if (kind == kRopeX) return launch_tc<64, kRopeX>(mk, mv, a, max_q, st);
   if (kind == kAlibi) return launch_tc<64, kAlibi>(mk, mv, a, max_q, st);
   return launch_tc<64, kNone>(mk, mv, a, max_q, st);
 }

@@ -53,18 +53,19 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4):
+    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3):
         """ntiles K/V tiles, nq live Q tiles (1 or 2), `clean(j)`: whether tile j has key-less
-        rows (used only by subclasses that model a V-cleaning role)."""
+        rows (used only by subclasses that model a V-cleaning role); kst K ring stages (the V
+        ring has 2); slots metadata slots."""
         self.rng = random.Random(seed)
         self.now = 0
         self.max_latency = self.rng.choice([0, 3, 12, 40])
         self.n, self.nq = ntiles, nq
         self.clean_of = clean or (lambda j: False)
-        self.slots = slots
-        self.K_FULL = [Bar(f"K_FULL{s}", 1) for s in range(2)]
-        self.K_READY = [Bar(f"K_READY{s}", 1) for s in range(2)]
-        self.K_FREE = [Bar(f"K_FREE{s}", 1) for s in range(2)]
+        self.slots, self.kst = slots, kst
+        self.K_FULL = [Bar(f"K_FULL{s}", 1) for s in range(kst)]
+        self.K_READY = [Bar(f"K_READY{s}", 1) for s in range(kst)]
+        self.K_FREE = [Bar(f"K_FREE{s}", 1) for s in range(kst)]
         self.V_FULL = [Bar(f"V_FULL{s}", 1) for s in range(2)]
         self.V_FREE = [Bar(f"V_FREE{s}", 1) for s in range(2)]
         self.S_FULL = [Bar(f"S_FULL{i}", 1) for i in range(2)]
@@ -74,9 +75,9 @@ class Sim:
         self.FINAL = Bar("FINAL", 1)
         # state for hazard checks
         self.slot_tile = [None] * self.slots
-        self.kstage = [None, None]          # tile whose K is in the stage (landed)
+        self.kstage = [None] * kst          # tile whose K is in the stage (landed)
         self.vstage = [None, None]
-        self.kstage_users = [set(), set()]  # outstanding consumers of the stage's tile
+        self.kstage_users = [set() for _ in range(kst)]  # outstanding consumers of the stage's tile
         self.vstage_users = [set(), set()]
         self.tma = []      # pending copies: (kind, stage, tile, bar, earliest landing step)
         self.pipe = []     # tensor pipe FIFO: ('mma', fn) or ('commit', bar)
@@ -99,7 +100,7 @@ class Sim:
 
     # ------------------------------------------------------------------ engines
     def issue_tma(self, kind, j, bar):
-        st = j % 2
+        st = j % (self.kst if kind == "K" else 2)
         users = self.kstage_users[st] if kind == "K" else self.vstage_users[st]
         if users:
             raise ProtocolError(f"{kind}({j}) issued into stage {st} while {sorted(users)} still use it")
@@ -112,6 +113,8 @@ class Sim:
         i = self.rng.choice(self.tma_ready())
         kind, st, j, bar, _ = self.tma.pop(i)
         if kind == "K":
+            if self.kstage_users[st]:
+                raise ProtocolError(f"K({j}) lands in stage {st} while {sorted(self.kstage_users[st])} still use it")
             self.kstage[st] = j
             self.kstage_users[st] = {"rot", "qk0"} | ({"qk1"} if self.nq == 2 else set())
         else:
@@ -129,7 +132,7 @@ class Sim:
     # ------------------------------------------------------------------ MMAs
     def qk(self, i, j, buf):
         def run():
-            st = j % 2
+            st = j % self.kst
             if self.kstage[st] != j or "rot" in self.kstage_users[st]:
                 raise ProtocolError(f"QK{i}({j}) reads K stage {st} holding {self.kstage[st]} "
                                     f"(rotated: {'rot' not in self.kstage_users[st]})")
@@ -168,9 +171,9 @@ class Sim:
         n = self.n
 
         def issue_k(j):  # wait for the stage, publish the tile's metadata, load K
-            s = j % 2
-            if j >= 2:
-                yield ("wait", self.K_FREE[s], j // 2 - 1)
+            s = j % self.kst
+            if j >= self.kst:
+                yield ("wait", self.K_FREE[s], j // self.kst - 1)
             self.publish(j)
             self.K_FULL[s].arrive(expect_tx=1)
             self.issue_tma("K", j, self.K_FULL[s])
@@ -185,17 +188,19 @@ class Sim:
             self.issue_tma("V", j, self.V_FULL[s])
             yield ("step",)
 
-        # issue order K0, K1, V0, K2, V1, ...
-        yield from issue_k(0)
+        # K runs kst - 1 tiles ahead of V: (kst = 3) K0, K1, K2, V0, K3, V1, ...
+        ahead = self.kst - 1
+        for j in range(min(ahead, n)):
+            yield from issue_k(j)
         for j in range(n):
-            if j + 1 < n:
-                yield from issue_k(j + 1)
+            if j + ahead < n:
+                yield from issue_k(j + ahead)
             yield from issue_v(j)
 
     def rotation(self):
         for j in range(self.n):
-            s = j % 2
-            yield ("wait", self.K_FULL[s], j // 2)
+            s = j % self.kst
+            yield ("wait", self.K_FULL[s], j // self.kst)
             self.read_slot(j, "rotation")
             yield ("step",)  # rotate in place
             if self.kstage[s] != j:
@@ -235,12 +240,12 @@ class Sim:
         yield ("wait", self.Q_READY, 0)
         if nq == 1:
             def qk1(j):
-                yield ("wait", self.K_READY[j % 2], j // 2)
+                yield ("wait", self.K_READY[j % self.kst], j // self.kst)
                 self.read_slot(j, "mma-qk1")
                 self.mma_saw(j)
                 self.qk(0, j, j & 1)
                 self.commit(self.S_FULL[j & 1])
-                self.commit(self.K_FREE[j % 2])
+                self.commit(self.K_FREE[j % self.kst])
 
             yield from qk1(0)
             if n > 1:
@@ -263,11 +268,11 @@ class Sim:
             self.commit(self.S_FULL[1])
             self.commit(self.K_FREE[0])
             for j in range(1, n):
-                s, sp = j % 2, (j - 1) % 2
+                s, sp = j % self.kst, (j - 1) % 2
                 yield ("wait", self.P_FULL[0], j - 1)
                 yield from self.mma_wait_v(j - 1)
                 self.pv(0, j - 1, 0)
-                yield ("wait", self.K_READY[s], j // 2)
+                yield ("wait", self.K_READY[s], j // self.kst)
                 self.read_slot(j, "mma-qk")
                 self.mma_saw(j)
                 self.qk(0, j, 0)

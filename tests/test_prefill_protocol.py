@@ -29,9 +29,10 @@ def _schedules(n_runs, seed0=0):
 
 @pytest.mark.parametrize("part", range(4))
 def test_protocol_as_built_is_safe_under_random_interleavings(part):
+    """The kernel's configuration: a 3-stage K ring, a 2-stage V ring, 6 metadata slots."""
     for seed, n, nq, clean in _schedules(500, seed0=500 * part):
         try:
-            pm.Sim(n, nq, CLEAN[clean], seed=seed).run()
+            pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=3, slots=6).run()
         except pm.ProtocolError as e:
             pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles: {e}")
 
@@ -46,17 +47,27 @@ def _caught(make, n_runs=200):
     return caught
 
 
+def test_two_stage_k_ring_is_safe_too():
+    for seed, n, nq, clean in _schedules(300, seed0=7000):
+        try:
+            pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=2, slots=4).run()
+        except pm.ProtocolError as e:
+            pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles: {e}")
+
+
 def test_model_catches_too_few_metadata_slots():
-    assert _caught(lambda n, nq, clean, seed: pm.Sim(n, nq, CLEAN[clean], seed=seed, slots=2)) > 0
+    """With the K ring two tiles ahead, the one-live-Q-tile schedule can publish tile j + 4's
+    metadata while the softmax of tile j still reads its slot: 4 slots are too few."""
+    assert _caught(lambda n, nq, clean, seed: pm.Sim(n, nq, CLEAN[clean], seed=seed, slots=4), 400) > 0
 
 
 def test_model_catches_v_stage_refilled_before_its_pv():
     class NoVFreeWait(pm.Sim):
         def producer(self):
             def issue_k(j):
-                s = j % 2
-                if j >= 2:
-                    yield ("wait", self.K_FREE[s], j // 2 - 1)
+                s = j % self.kst
+                if j >= self.kst:
+                    yield ("wait", self.K_FREE[s], j // self.kst - 1)
                 self.publish(j)
                 self.K_FULL[s].arrive(expect_tx=1)
                 self.issue_tma("K", j, self.K_FULL[s])
@@ -69,10 +80,12 @@ def test_model_catches_v_stage_refilled_before_its_pv():
                 self.issue_tma("V", j, self.V_FULL[s])
                 yield ("step",)
 
-            yield from issue_k(0)
+            ahead = self.kst - 1
+            for j in range(min(ahead, self.n)):
+                yield from issue_k(j)
             for j in range(self.n):
-                if j + 1 < self.n:
-                    yield from issue_k(j + 1)
+                if j + ahead < self.n:
+                    yield from issue_k(j + ahead)
                 yield from issue_v(j)
 
     assert _caught(lambda n, nq, clean, seed: NoVFreeWait(n, nq, CLEAN[clean], seed=seed)) > 0
@@ -123,20 +136,20 @@ class OldVClean(pm.Sim):
 
     def rotation(self):
         for j in range(self.n):
-            s = j % 2
-            yield ("wait", self.K_FULL[s], j // 2)
+            s, sv = j % self.kst, j % 2
+            yield ("wait", self.K_FULL[s], j // self.kst)
             self.read_slot(j, "rotation")
             yield ("step",)
             self.kstage_users[s].discard("rot")
             self.K_READY[s].arrive()
             if self.clean_of(j) or self.every_phase:
-                yield ("wait", self.V_FULL[s], j // 2)
-                if self.vstage[s] != j:
-                    raise pm.ProtocolError(f"V clean of tile {j} finds stage holding {self.vstage[s]}")
+                yield ("wait", self.V_FULL[sv], j // 2)
+                if self.vstage[sv] != j:
+                    raise pm.ProtocolError(f"V clean of tile {j} finds stage holding {self.vstage[sv]}")
                 if self.clean_of(j):
                     yield ("step",)
-                    self.vstage_users[s].discard("clean")
-                    self.V_READY[s].arrive()
+                    self.vstage_users[sv].discard("clean")
+                    self.V_READY[sv].arrive()
 
     def mma_wait_v(self, jj):
         s = jj % 2
@@ -155,7 +168,7 @@ def test_model_catches_the_old_v_clean_handshake():
     caught = []
     for seed, n, nq, clean in _schedules(400):
         try:
-            OldVClean(n, nq, CLEAN[clean], seed=seed).run()
+            OldVClean(n, nq, CLEAN[clean], seed=seed, kst=2).run()
         except pm.ProtocolError as e:
             caught.append(str(e))
     assert caught, "the model let the old V-clean handshake through"
@@ -166,7 +179,7 @@ def test_v_clean_consuming_every_phase_is_safe():
     """Control for the test above: the model does not reject a V-cleaning role as such."""
     for seed, n, nq, clean in _schedules(400):
         try:
-            OldVCleanEveryPhase(n, nq, CLEAN[clean], seed=seed).run()
+            OldVCleanEveryPhase(n, nq, CLEAN[clean], seed=seed, kst=2).run()
         except pm.ProtocolError as e:
             pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles, clean={clean}: {e}")
 
