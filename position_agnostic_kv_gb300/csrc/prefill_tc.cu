@@ -249,6 +249,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 }
 
 // ---------------------------------------------------------------- the kernel
+__device__ __forceinline__ float max3f(float a, float b, float c) {  // three-input maximum
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {  // 2^x on the MUFU (approx, flush-to-zero)
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -478,24 +484,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             }
           }
         }
-        float mx = -INFINITY;
+        // row max over 128 scores: eight independent runs of three-input maxima, then a tree
+        float mq[8];
 #pragma unroll
-        for (int e = 0; e < kN; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        for (int q = 0; q < 8; ++q) {
+          const float* x = reinterpret_cast<const float*>(v + 16 * q);
+          float m = max3f(x[0], x[1], x[2]);
+#pragma unroll
+          for (int e = 3; e < 15; e += 2) m = max3f(m, x[e], x[e + 1]);
+          mq[q] = fmaxf(m, x[15]);
+        }
+        const float mx = max3f(max3f(mq[0], mq[1], mq[2]), max3f(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
         const bool need = mx > m_run + kTau;
         const float m_new = need ? mx : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
         const float2 mneg = make_float2(-m_use, -m_use);
-        float2 sum2 = make_float2(0.f, 0.f);
+        float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};  // four independent partial sums
         // P packed to bf16 pairs in place: pair e (keys 2e, 2e+1) lands in v[e] (already consumed)
 #pragma unroll
         for (int e = 0; e < kN / 2; ++e) {
           float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
           x = __fadd2_rn(x, mneg);
           const float2 ev = make_float2(ex2(x.x), ex2(x.y));
-          sum2 = __fadd2_rn(sum2, ev);
+          sum4[e & 3] = __fadd2_rn(sum4[e & 3], ev);
           v[e] = f2_to_bf2(ev.x, ev.y);
         }
-        const float sum = sum2.x + sum2.y;
+        const float2 s01 = __fadd2_rn(sum4[0], sum4[1]), s23 = __fadd2_rn(sum4[2], sum4[3]);
+        const float2 s03 = __fadd2_rn(s01, s23);
+        const float sum = s03.x + s03.y;
         const float alpha = (j > 0 && need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
         l_run = (j == 0) ? sum : l_run * alpha + sum;
         // O rescale needs the previous tile's PV complete: with two Q tiles the S commit waited
