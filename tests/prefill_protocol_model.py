@@ -53,16 +53,17 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3):
+    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3, vprod=False):
         """ntiles K/V tiles, nq live Q tiles (1 or 2), `clean(j)`: whether tile j has key-less
         rows (used only by subclasses that model a V-cleaning role); kst K ring stages (the V
-        ring has 2); slots metadata slots."""
+        ring has 2); slots metadata slots; vprod: V is issued by a producer of its own, which
+        reads the block words itself (no metadata slot)."""
         self.rng = random.Random(seed)
         self.now = 0
         self.max_latency = self.rng.choice([0, 3, 12, 40])
         self.n, self.nq = ntiles, nq
         self.clean_of = clean or (lambda j: False)
-        self.slots, self.kst = slots, kst
+        self.slots, self.kst, self.vprod = slots, kst, vprod
         self.K_FULL = [Bar(f"K_FULL{s}", 1) for s in range(kst)]
         self.K_READY = [Bar(f"K_READY{s}", 1) for s in range(kst)]
         self.K_FREE = [Bar(f"K_FREE{s}", 1) for s in range(kst)]
@@ -179,15 +180,6 @@ class Sim:
             self.issue_tma("K", j, self.K_FULL[s])
             yield ("step",)
 
-        def issue_v(j):  # wait for the stage; clear empty page slots; load V
-            s = j % 2
-            if j >= 2:
-                yield ("wait", self.V_FREE[s], j // 2 - 1)
-            self.read_slot(j, "issue_v")
-            self.V_FULL[s].arrive(expect_tx=1)
-            self.issue_tma("V", j, self.V_FULL[s])
-            yield ("step",)
-
         # K runs kst - 1 tiles ahead of V: (kst = 3) K0, K1, K2, V0, K3, V1, ...
         ahead = self.kst - 1
         for j in range(min(ahead, n)):
@@ -195,7 +187,22 @@ class Sim:
         for j in range(n):
             if j + ahead < n:
                 yield from issue_k(j + ahead)
-            yield from issue_v(j)
+            if not self.vprod:
+                yield from self.issue_v(j, from_slot=True)
+
+    def issue_v(self, j, from_slot):  # wait for the stage; clear empty page slots; load V
+        s = j % 2
+        if j >= 2:
+            yield ("wait", self.V_FREE[s], j // 2 - 1)
+        if from_slot:
+            self.read_slot(j, "issue_v")
+        self.V_FULL[s].arrive(expect_tx=1)
+        self.issue_tma("V", j, self.V_FULL[s])
+        yield ("step",)
+
+    def vproducer(self):
+        for j in range(self.n):
+            yield from self.issue_v(j, from_slot=False)
 
     def rotation(self):
         for j in range(self.n):
@@ -295,8 +302,11 @@ class Sim:
 
     # ------------------------------------------------------------------ scheduler
     def actors(self):
-        return {"producer": self.producer(), "rotation": self.rotation(), "mma": self.mma(),
-                "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+        a = {"producer": self.producer(), "rotation": self.rotation(), "mma": self.mma(),
+             "softmax0": self.softmax(0), "softmax1": self.softmax(1)}
+        if self.vprod:
+            a["vproducer"] = self.vproducer()
+        return a
 
     def run(self, max_steps=200000):
         actors = self.actors()
