@@ -70,6 +70,8 @@ def parse_args():
     p.add_argument("--extra", default="rag8b", help="comma-separated workloads also timed (sub-objects)")
     p.add_argument("--overhead-reps", type=int, default=20, help="timed launches per overhead variant")
     p.add_argument("--sharing", choices=["private", "shared"], default="private")
+    p.add_argument("--batch", type=int, default=None,
+                   help="keep only the first requests of --workload (smaller cases for profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of graph replay")
@@ -219,7 +221,7 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
     from workloads import make_workload
 
     dev = torch.device("cuda", dist.local_rank)
-    w = make_workload(name, sharing=sharing)
+    w = make_workload(name, sharing=sharing, batch=args.batch if name == args.workload else None)
     pb, pre, decs, in_blob, out_blob, out_p, outs_d = _prepare(w, dev, args.pos)
     n_dec = w.n_decode
     stream = torch.cuda.Stream(device=dev)
@@ -363,7 +365,8 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
                     "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_med * 1e3}
     res = {
         "value": value, "ms_per_step": mean_ms, "tokens_per_step": tokens_per_step,
-        "workload": f"{name}: {WORKLOAD_TEXT[name]}", "sharing": sharing, "pos": args.pos or w.pos.kind,
+        "workload": f"{name}: {WORKLOAD_TEXT[name]}" + (f" (first {w.B} requests)" if w.B != make_workload(
+            name, sharing=sharing).B else ""), "sharing": sharing, "pos": args.pos or w.pos.kind,
         "global_batch": w.B * dist.world, "seq_len": int(keys0.max()) + n_dec,
         "launch": "CUDA graph per step" if graph is not None else "eager",
         "roofline": roofline,
@@ -476,7 +479,7 @@ def run_ours(args, dist):
     if ovh:
         res["rotation_overhead"] = ovh
     extra = {}
-    for name in [x for x in args.extra.split(",") if x and x != args.workload]:
+    for name in [x for x in args.extra.split(",") if x and x not in ("none", args.workload)]:
         e = measure_step(args, dist, lk, name, args.sharing, min(args.steps, 20), args.warmup,
                          overhead=not args.no_overhead)
         extra[name] = {k: e[k] for k in ("value", "ms_per_step", "tokens_per_step", "workload", "decode",
