@@ -64,6 +64,7 @@ constexpr int kThreads = 512;
 constexpr int kRotWarp0 = 8;
 constexpr int kProdWarp = 12;
 constexpr int kMmaWarp = 13;
+constexpr int kVProdWarp = 14;  // V producer of the SPLIT_V instantiation
 // Registers per thread after the re-split, per warpgroup role (the splits with no spills):
 // kernels that rotate K give the rotation warps more (2*128*184 + 128*56 + 128*88), the others
 // give the softmax more (2*128*192 + 128*48 + 128*80); both add up to 512 * 128 = 65536.
@@ -261,7 +262,12 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the MUFU (approx, flu
   return y;
 }
 
-template <int D, int POS>
+// SPLIT_V: with one live Q tile, V is issued by warp 14 with its own barrier chain instead of
+// being interleaved behind K by warp 12.  Chosen on the host for long one-Q-tile key ranges
+// (decode mode, long-context prefill with short queries), where V copies queued behind K leave
+// the ingest short; the two-Q-tile schedule keeps one producer.  A separate instantiation, so
+// each schedule's code is generated on its own.
+template <int D, int POS, bool SPLIT_V>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
   using L = Layout<D>;
@@ -812,10 +818,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       };
       // K runs kKStages - 1 tiles ahead of V: K0 K1 K2 V0 K3 V1 ...
       bool ok = true;
+      const bool own_v = !(SPLIT_V && nq == 1);  // otherwise warp 14 issues V
       for (int j = 0; j < kKStages - 1 && j < ntiles && ok; ++j) ok = issue_k(j);
       for (int j = 0; j < ntiles && ok; ++j) {
         if (j + kKStages - 1 < ntiles) ok = issue_k(j + kKStages - 1);
-        if (ok) ok = issue_v(j);
+        if (ok && own_v) ok = issue_v(j);
       }
       // never leave copies in flight: wait (bounded) for the last loads of every stage
       if (lane == 0) {
@@ -832,6 +839,69 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           }
         }
       }
+    } else if (SPLIT_V && warp == kVProdWarp && nq == 1) {
+      // ============================ V producer (one live Q tile)
+      // V's own producer (SPLIT_V): it reads the block words itself; pages, rows and zero fill
+      // follow the K producer's rules, and issue_v's stage protocol.
+      const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks;
+      auto tile_of = [&](int j) { return POS == kAlibi ? t0 + ntiles - 1 - j : t0 + j; };
+      auto fetch = [&](int j) -> uint64_t {
+        const int jb = tile_of(j) * kPagesPerTile + lane;
+        return (lane < kPagesPerTile && j < ntiles && jb < nb) ? ldg_u64(mrow + jb) : 0ull;
+      };
+      uint64_t w_next = fetch(0);
+      int issued_v = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % kVStages;
+        const uint64_t w = w_next;
+        w_next = fetch(j + 1);
+        int rows = 0, zc = 0;
+        const int jb = tile_of(j) * kPagesPerTile + lane;
+        if (lane < kPagesPerTile && jb < nb) {
+          const int page = int(word_page(w));
+          const int start = int(word_delta(w)) + kPage * int(word_pg(w));
+          rows = max(0, min(min(int(word_nvalid(w)), kPage), m_max - start + 1));
+          if (page >= a.num_pages) rows = 0;  // reported by the K producer
+          zc = page * a.Hkv + g;
+        }
+        const int lo = kPage - rows;
+        if (j >= kVStages) {
+          const bool freed = wait_bar(BAR(B_V_FREE + s), uint32_t(((j / kVStages) - 1) & 1), abort_flag, a.status);
+          if (!__all_sync(0xffffffffu, freed)) break;
+        }
+        const uint32_t sV = sV0 + uint32_t(s * L::TILE);
+        const uint32_t loaded = __ballot_sync(0xffffffffu, lane < kPagesPerTile && rows > 0);
+        const uint32_t empty = ~loaded & ((1u << kPagesPerTile) - 1u);
+        if (empty) {  // page slots past the last block: cleared (they meet PV with zero weights)
+          for (int pp = 0; pp < kPagesPerTile; ++pp) {
+            if (!((empty >> pp) & 1u)) continue;
+#pragma unroll
+            for (int cb = 0; cb < L::CB; ++cb)
+#pragma unroll
+              for (int i = 0; i < kPage * 8 / 32; ++i) {
+                const int row = pp * kPage + (i * 32 + lane) / 8, c = (i * 32 + lane) % 8;
+                st_shared_v4(sV + uint32_t(cb * L::BLK) + swz(row, c), make_uint4(0, 0, 0, 0));
+              }
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(BAR(B_V_FULL + s), uint32_t(__popc(loaded)) * kPage * D * 2);
+        __syncwarp();
+        if (lane < kPagesPerTile && rows > 0)
+#pragma unroll
+          for (int cb = 0; cb < L::CB; ++cb)
+            tma_load_3d(sV + uint32_t(cb * L::BLK + lane * kPage * 128), &tmv, cb * 64, -lo, zc, BAR(B_V_FULL + s));
+        __syncwarp();
+        issued_v = j + 1;
+      }
+      if (lane == 0)  // never leave copies in flight
+        for (int j = max(0, issued_v - kVStages); j < issued_v; ++j) {
+          const uint32_t bar = BAR(B_V_FULL + j % kVStages), par = uint32_t((j / kVStages) & 1);
+          WaitClock clk;
+          while (!mbar_test(bar, par) && !clk.expired()) {
+          }
+        }
     } else if (warp == kMmaWarp) {
       // ============================ MMA issue (one thread)
       if (lane == 0) {
@@ -1001,11 +1071,11 @@ static int cache_map(CUtensorMap* map, const void* base, int num_pages, int Hkv,
   return LAZY_OK;
 }
 
-template <int D, int POS>
+template <int D, int POS, bool SPLIT_V>
 static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q, cudaStream_t st) {
   // (decode mode: max_q = 1, one query row per request)
   using L = tc::Layout<D>;
-  auto kern = tc::prefill_tc_kernel<D, POS>;
+  auto kern = tc::prefill_tc_kernel<D, POS, SPLIT_V>;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1030,6 +1100,21 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
   dim3 grid(unsigned((max_q + rows_tok - 1) / rows_tok) * unsigned(a.S), a.Hkv, a.B);
   LAZY_CUDA_TRY(launch_pdl(kern, grid, dim3(tc::kThreads), L::SMEM, st, mk, mv, a));
   return LAZY_OK;
+}
+
+template <bool SPLIT_V>
+static int dispatch_tc(int D, int kind, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q,
+                       cudaStream_t st) {
+  if (D == 128) {
+    if (kind == kRope) return launch_tc<128, kRope, SPLIT_V>(mk, mv, a, max_q, st);
+    if (kind == kRopeX) return launch_tc<128, kRopeX, SPLIT_V>(mk, mv, a, max_q, st);
+    if (kind == kAlibi) return launch_tc<128, kAlibi, SPLIT_V>(mk, mv, a, max_q, st);
+    return launch_tc<128, kNone, SPLIT_V>(mk, mv, a, max_q, st);
+  }
+  if (kind == kRope) return launch_tc<64, kRope, SPLIT_V>(mk, mv, a, max_q, st);
+  if (kind == kRopeX) return launch_tc<64, kRopeX, SPLIT_V>(mk, mv, a, max_q, st);
+  if (kind == kAlibi) return launch_tc<64, kAlibi, SPLIT_V>(mk, mv, a, max_q, st);
+  return launch_tc<64, kNone, SPLIT_V>(mk, mv, a, max_q, st);
 }
 
 int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
@@ -1068,16 +1153,14 @@ int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, c
   // interleaved pairs take the generic rotation (kRopeX)
   int kind = (pos.kind == kYarn) ? kRope : pos.kind;
   if (kind == kRope && (pos.rotary_dim != D || pos.interleaved)) kind = kRopeX;
-  if (D == 128) {
-    if (kind == kRope) return launch_tc<128, kRope>(mk, mv, a, max_q, st);
-    if (kind == kRopeX) return launch_tc<128, kRopeX>(mk, mv, a, max_q, st);
-    if (kind == kAlibi) return launch_tc<128, kAlibi>(mk, mv, a, max_q, st);
-    return launch_tc<128, kNone>(mk, mv, a, max_q, st);
-  }
-  if (kind == kRope) return launch_tc<64, kRope>(mk, mv, a, max_q, st);
-  if (kind == kRopeX) return launch_tc<64, kRopeX>(mk, mv, a, max_q, st);
-  if (kind == kAlibi) return launch_tc<64, kAlibi>(mk, mv, a, max_q, st);
-  return launch_tc<64, kNone>(mk, mv, a, max_q, st);
+  // A separate V producer when every CTA has one live Q tile (its tokens fit one 128-row tile)
+  // and a long key range: at least 20 tiles of 128 keys per CTA.  Measured on GB300 (same-box
+  // A/B): MQA decode 53.2 -> 49.6 us, yarn8b prefill 340 -> 323-330 us; rag8b's 16-tile CTAs
+  // were slower with it.
+  const int tiles_per_cta = ((max_blocks + tc::kPagesPerTile - 1) / tc::kPagesPerTile + S - 1) / S;
+  const bool split_v = (seq_len != nullptr || max_q <= tc::kM / G) && tiles_per_cta >= 20;
+  if (split_v) return dispatch_tc<true>(D, kind, mk, mv, a, max_q, st);
+  return dispatch_tc<false>(D, kind, mk, mv, a, max_q, st);
 }
 
 }  // namespace lazykv

@@ -30,7 +30,7 @@ def _schedules(n_runs, seed0=0):
 @pytest.mark.parametrize("part", range(4))
 def test_protocol_as_built_is_safe_under_random_interleavings(part):
     """The kernel's configuration: a 3-stage K ring, a 2-stage V ring, 6 metadata slots, one
-    producer issuing K and V."""
+    producer issuing K and V (the instantiation without SPLIT_V, and every two-Q-tile CTA)."""
     for seed, n, nq, clean in _schedules(500, seed0=500 * part):
         try:
             pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=3, slots=6).run()
@@ -49,8 +49,8 @@ def _caught(make, n_runs=200):
 
 
 def test_separate_v_producer_is_safe_for_both_schedules():
-    """The variant with V issued by a warp of its own (measured, not built: it sped up long
-    one-Q-tile ranges but slowed the 70B prefill) has a safe protocol too."""
+    """V issued by a warp of its own that reads the block words itself: the SPLIT_V
+    instantiation (one-Q-tile CTAs over long key ranges); safe for both schedules."""
     for seed, n, nq, clean in _schedules(300, seed0=9000):
         try:
             pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=3, slots=6, vprod=True).run()
