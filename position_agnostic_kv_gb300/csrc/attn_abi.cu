@@ -101,5 +101,5 @@ extern "C" size_t lazy_workspace_size(int phase, int rows, int B, int max_blocks
   if (phase != LAZY_PHASE_PREFILL) return 0;
   const int G = Hq / Hkv;
   if (G <= 128 && 128 % G == 0) return 0;  // the tensor-core prefill needs no workspace
-  return decode_ws_bytes(rows, Hq, Hkv, D, max_blocks);
+  return decode_ws_bytes(rows, Hq, Hkv, D, max_blocks, true);
 }

@@ -30,7 +30,6 @@
 
 namespace lazykv {
 
-constexpr int kDecWarps = 4;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (base-2 units)
 
 
@@ -60,7 +59,7 @@ struct RowReduce {
   }
 };
 
-template <int D, int G, int NST>
+template <int D, int G, int NST, int NW>  // NW warps per CTA
 struct DecLayout {
   static constexpr int LPR = D / 8;             // lanes per row
   static constexpr int RPI = 32 / LPR;          // rows per warp-wide load
@@ -70,19 +69,23 @@ struct DecLayout {
   static constexpr int DUP = V >= LPR ? 1 : LPR / V;  // lanes holding the same score
   static constexpr int PAGE_BYTES = kPage * D * 2;
   static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
-  static constexpr int STAGES_BYTES = kDecWarps * NST * STAGE_BYTES;
+  static constexpr int STAGES_BYTES = NW * NST * STAGE_BYTES;
   static constexpr int QS_OFF = STAGES_BYTES;                 // q_raw fp32 [G][D]
   static constexpr int PB_OFF = QS_OFF + G * D * 4;           // p buffer [warp][16][G]
-  static constexpr int SLOT_OFF = PB_OFF + kDecWarps * kPage * G * 4;  // [warp][NST] {u64 word, i32 rows}
-  static constexpr int BAR_OFF = SLOT_OFF + kDecWarps * NST * 16;
-  static constexpr int SMEM = BAR_OFF + kDecWarps * NST * 8;
+  static constexpr int SLOT_OFF = PB_OFF + NW * kPage * G * 4;  // [warp][NST] {u64 word, i32 rows}
+  static constexpr int BAR_OFF = SLOT_OFF + NW * NST * 16;
+  static constexpr int SMEM = BAR_OFF + NW * NST * 8;
   // after the page loop the stage area is reused to merge warps: [warp][G][D] o, [warp][G][2] m,l
-  static_assert(kDecWarps * G * (D + 2) * 4 <= STAGES_BYTES, "merge buffer must fit in the stages");
+  static_assert(NW * G * (D + 2) * 4 <= STAGES_BYTES, "merge buffer must fit in the stages");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, int G, int POS, bool ROWS, int NST>
-__global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kernel(const DecodeArgs a) {
-  using L = DecLayout<D, G, NST>;
+// NW = 4: the general shape, several CTAs per SM (3 for head groups of at most 4).
+// NW = 12: one CTA per SM for launches whose (row, head group) units fit on the SMs (small
+// batches): each unit gets a whole SM, so no SM holds more work than another.
+template <int D, int G, int POS, bool ROWS, int NST, int NW>
+__global__ void __launch_bounds__(NW * 32, (NW == 4 && G <= 4) ? 3 : 1) decode_kernel(const DecodeArgs a) {
+  using L = DecLayout<D, G, NST, NW>;
   constexpr int LPR = L::LPR, RPI = L::RPI, RPL = L::RPL, V = L::V, E = L::E;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
   const int chunk = (nb + a.S - 1) / a.S;
   const int beg = split * chunk, end = min(nb, beg + chunk);
   const int len = max(0, end - beg);
-  const int wch = (len + kDecWarps - 1) / kDecWarps;
+  const int wch = (len + NW - 1) / NW;
   const int wb = beg + warp * wch;
   const int n = max(0, min(end, wb + wch) - wb);
 
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
   }
   __syncthreads();  // every stage consumed: reuse the stage area
   float* mo = reinterpret_cast<float*>(smem);                  // [warp][G][D]
-  float* mml = mo + kDecWarps * G * D;                           // [warp][G][2]
+  float* mml = mo + NW * G * D;                                  // [warp][G][2]
   if (lane < LPR) {
 #pragma unroll
     for (int h = 0; h < G; ++h)
@@ -433,11 +436,11 @@ __global__ void __launch_bounds__(kDecWarps * 32, (G <= 4 ? 3 : 1)) decode_kerne
     const int h = t / D, col = t % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w2 = 0; w2 < kDecWarps; ++w2) M = fmaxf(M, mml[(w2 * G + h) * 2]);
+    for (int w2 = 0; w2 < NW; ++w2) M = fmaxf(M, mml[(w2 * G + h) * 2]);
     float Ov = 0.f, Lv = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w2 = 0; w2 < kDecWarps; ++w2) {
+      for (int w2 = 0; w2 < NW; ++w2) {
         const float mw = mml[(w2 * G + h) * 2];
         const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
         Ov += sc * mo[(w2 * G + h) * D + col];
@@ -498,15 +501,29 @@ int decode_group(int Hq, int Hkv) {
   return G >= 8 ? 8 : G;  // heads per CTA (MQA: several CTAs share one KV head)
 }
 
-int choose_splits(int rows, int Hq, int Hkv, int max_blocks) {
+// Warps per CTA and KV splits of the CUDA-core decode.
+DecodeShape decode_shape(int rows, int Hq, int Hkv, int max_blocks) {
   const int G = decode_group(Hq, Hkv);
   const long long units = (long long)rows * (Hq / G);
-  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // CTAs resident at once
+  const int sms = sm_count();
+  // Small batches whose (row, head group) units fill between half and all of the SMs: one
+  // 12-warp CTA per unit, no key split.  Every SM then carries the same load (three 4-warp CTAs
+  // on some SMs and two on others did not), and there is no partial to merge.  Fewer units are
+  // better served by 4-warp CTAs split over more SMs.
+  if (G <= 4 && units <= sms && 2 * units > sms && max_blocks >= 12 * 4) return {12, 1};
+  return {4, choose_splits_rows(rows, Hq, Hkv, max_blocks)};
+}
+
+// Splits of the 4-warp shape (also the CUDA-core prefill's row mode, one query row per unit).
+int choose_splits_rows(int rows, int Hq, int Hkv, int max_blocks) {
+  const int G = decode_group(Hq, Hkv);
+  const long long units = (long long)rows * (Hq / G);
+  const long long slots = (long long)sm_count() * (G <= 4 ? 3 : 2);  // 4-warp CTAs resident at once
   // About 4 waves of resident CTAs, but runs of about 16 pages per warp: measured on GB300,
   // long per-warp page runs beat more, shorter CTAs (every CTA pays a pipeline start-up and its
   // split partials), and a partial last wave costs little once there are several waves.
   const long long want = (4 * slots + units - 1) / units;
-  const int max_by_len = max(1, (max_blocks + kDecWarps * 16 - 1) / (kDecWarps * 16));
+  const int max_by_len = max(1, (max_blocks + 4 * 16 - 1) / (4 * 16));
   long long s = want < max_by_len ? want : max_by_len;
   if (s < 1) s = 1;
   if (s > 64) s = 64;
@@ -533,19 +550,20 @@ int tc_decode_splits(int B, int Hkv, int max_blocks) {
   return int(s);
 }
 
-size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks) {
-  const int S = use_tc_decode(Hq, Hkv, D) ? tc_decode_splits(rows, Hkv, max_blocks)
-                                          : choose_splits(rows, Hq, Hkv, max_blocks);
+size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks, bool rows_mode) {
+  const int S = rows_mode                    ? choose_splits_rows(rows, Hq, Hkv, max_blocks)
+                : use_tc_decode(Hq, Hkv, D) ? tc_decode_splits(rows, Hkv, max_blocks)
+                                            : decode_shape(rows, Hq, Hkv, max_blocks).S;
   if (S <= 1) return 0;
   const size_t po = (size_t)rows * Hq * S * D * 4;
   const size_t pml = (size_t)rows * Hq * S * 2 * 4;
   return ((po + 255) / 256) * 256 + pml;
 }
 
-template <int D, int G, int POS, bool ROWS>
-static int launch_t(const DecodeArgs& a, cudaStream_t st) {
-  using L = DecLayout<D, G, kNst>;
-  auto kern = decode_kernel<D, G, POS, ROWS, kNst>;
+template <int D, int G, int POS, bool ROWS, int NW>
+static int launch_nw(const DecodeArgs& a, cudaStream_t st) {
+  using L = DecLayout<D, G, kNst, NW>;
+  auto kern = decode_kernel<D, G, POS, ROWS, kNst, NW>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -554,11 +572,18 @@ static int launch_t(const DecodeArgs& a, cudaStream_t st) {
     attr_set[dev & 63] = true;
   }
   dim3 grid(a.S, a.Hq / G, a.rows);
-  LAZY_CUDA_TRY(launch_pdl(kern, grid, dim3(kDecWarps * 32), L::SMEM, st, a));
+  LAZY_CUDA_TRY(launch_pdl(kern, grid, dim3(NW * 32), L::SMEM, st, a));
   if (a.S > 1)
     LAZY_CUDA_TRY(launch_pdl(merge_kernel<D>, dim3((unsigned)a.rows * a.Hq), dim3(D), 0, st,
                              (const float*)a.part_o, (const float*)a.part_ml, a.S, a.Hq, a.out, a.lse));
   return LAZY_OK;
+}
+
+template <int D, int G, int POS, bool ROWS>
+static int launch_t(const DecodeArgs& a, cudaStream_t st) {
+  if constexpr (G <= 4 && !ROWS)
+    if (a.nw == 12) return launch_nw<D, G, POS, ROWS, 12>(a, st);
+  return launch_nw<D, G, POS, ROWS, 4>(a, st);
 }
 
 template <int D, int G, bool ROWS>
@@ -588,7 +613,7 @@ int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_by
   if (!rows_mode && use_tc_decode(a.Hq, a.Hkv, D)) {
     a.S = tc_decode_splits(a.rows, a.Hkv, a.max_blocks);
     if (a.S > 1) {
-      const size_t need = decode_ws_bytes(a.rows, a.Hq, a.Hkv, D, a.max_blocks);
+      const size_t need = decode_ws_bytes(a.rows, a.Hq, a.Hkv, D, a.max_blocks, false);
       if (!ws || ws_bytes < need)
         return fail(LAZY_EINVAL, "workspace too small: need %zu bytes, got %zu", need, ws_bytes);
       if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(LAZY_EINVAL, "workspace must be 256-byte aligned");
@@ -611,9 +636,12 @@ int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_by
   a.group = decode_group(a.Hq, a.Hkv);
   const int G = a.Hq / a.Hkv;
   if (G % a.group != 0) return fail(LAZY_EINVAL, "Hq/Hkv = %d not supported", G);
-  a.S = choose_splits(a.rows, a.Hq, a.Hkv, a.max_blocks);
+  const DecodeShape shp = rows_mode ? DecodeShape{4, choose_splits_rows(a.rows, a.Hq, a.Hkv, a.max_blocks)}
+                                    : decode_shape(a.rows, a.Hq, a.Hkv, a.max_blocks);
+  a.nw = shp.nw;
+  a.S = shp.S;
   if (a.S > 1) {
-    const size_t need = decode_ws_bytes(a.rows, a.Hq, a.Hkv, D, a.max_blocks);
+    const size_t need = decode_ws_bytes(a.rows, a.Hq, a.Hkv, D, a.max_blocks, rows_mode);
     if (!ws || ws_bytes < need)
       return fail(LAZY_EINVAL, "workspace too small: need %zu bytes, got %zu", need, ws_bytes);
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(LAZY_EINVAL, "workspace must be 256-byte aligned");

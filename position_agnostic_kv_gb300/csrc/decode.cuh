@@ -16,6 +16,7 @@ struct DecodeArgs {
   const __nv_bfloat16* v_cache;
   int num_pages, B, max_blocks, Hq, Hkv, rows;
   int group;  // query heads per CTA (divides Hq / Hkv)
+  int nw;     // warps per CTA (4, or 12 for small batches)
   __nv_bfloat16* out;
   float* lse;
   float* part_o;   // [rows][Hq][S][D]
@@ -26,7 +27,14 @@ struct DecodeArgs {
 };
 
 int run_decode_rows(DecodeArgs& a, int D, bool rows_mode, void* ws, size_t ws_bytes, cudaStream_t st);
-size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks);
+struct DecodeShape {
+  int nw;  // warps per CTA
+  int S;   // KV splits per (row, head group)
+};
+DecodeShape decode_shape(int rows, int Hq, int Hkv, int max_blocks);
+int choose_splits_rows(int rows, int Hq, int Hkv, int max_blocks);
+// Workspace bytes of a decode (rows_mode = false) or of the CUDA-core prefill row mode.
+size_t decode_ws_bytes(int rows, int Hq, int Hkv, int D, int max_blocks, bool rows_mode = false);
 int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
                    const uint64_t* meta, int B, int max_blocks, int max_q, const void* k_cache,
                    const void* v_cache, int num_pages, int Hq, int Hkv, int D, const PosParams& pos, void* out,

@@ -494,8 +494,9 @@ def test_bad_page_sets_status_and_skips(lk):
 
 
 def test_workspace_too_small_is_rejected(lk):
+    """A batch whose decode splits the key range needs a workspace; 256 bytes is refused."""
     import torch
-    w = make_workload("rag8b", batch=16)
+    w = make_workload("yarn8b", batch=20)
     pb = _batch(w)
     pb.ws = torch.empty(256, dtype=torch.uint8, device="cuda")
     with pytest.raises(lk.LazyError, match="workspace"):

@@ -10,7 +10,7 @@ This test calls that entry point through the C ABI and checks it against lazy_at
 (with a caller workspace) on the same inputs, on two calls in a row: the second call reuses
 the array the first one left behind.  Both calls run the same kernels on the same inputs, so
 their outputs must be bit-identical.  Two head groupings: 4 heads per KV head (the CUDA-core
-decode and its split merge) and 32 (MQA: the tensor-core decode, its key range split over CTAs
+decode split over the key range, 20 requests of the YaRN workload, and its merge) and 32 (MQA: the tensor-core decode, its key range split over CTAs
 and merged).  It lives in a file of its own, collected last, so that a run stopping at the
 first failure has run every other test first; it needs nothing from them.
 """
@@ -25,13 +25,13 @@ from workloads import make_workload
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name,batch", [("rag8b", 16), ("mqa_alibi", 4)])
+@pytest.mark.parametrize("name,batch", [("yarn8b", 20), ("mqa_alibi", 4)])
 def test_noalloc_decode_matches_workspace_decode_on_two_calls(name, batch):
     import torch
     lk = lib()
     from position_agnostic_kv_gb300.runner import PagedBatch
 
-    w = make_workload(name, batch=batch)  # every request over ~2 000 or ~12 000 keys
+    w = make_workload(name, batch=batch)  # every request over ~12 000 keys
     pb = PagedBatch(w, device="cuda")
     need = lk.workspace_size(lk.PHASE_DECODE, w.B, w.B, pb.max_blocks, w.Hq, w.Hkv, w.D)
     assert need > 0, "this batch must use split scratch for the test to mean anything"
