@@ -17,7 +17,10 @@
  *     beyond one 32-bit device status word per GPU (see lazy_device_status).
  *   - bf16 tensors are contiguous, row-major, 16-byte aligned.
  *   - Paged caches: k_cache and v_cache are bf16 [num_pages][Hkv][16][D]; one page of one KV
- *     head is 16 * D * 2 bytes, contiguous.  A cache slot is page * 16 + row.
+ *     head is 16 * D * 2 bytes, contiguous.  A cache slot is page * 16 + row.  The attention
+ *     kernels read only rows that hold a key the query can see (a block's first n_valid rows,
+ *     and in the query segment none past the query's position), so the rest of a page may hold
+ *     anything, uninitialised or NaN bits included.
  *   - Every GPU entry point is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream), performs no synchronisation and returns after the launch.
  *   - Kernels are launched with programmatic dependent launch: one may become resident while
@@ -112,7 +115,7 @@ typedef struct lazy_pos_cfg {
  *                document pg (< 2048), [39:16] Delta (< 2^24), [63:40] physical page (< 2^24).
  *                Key row t of a block sits at absolute position p = Delta + 16 * pg + t.
  *                Query-segment blocks are listed as full (n_valid = 16); causality (p <= m)
- *                masks their unwritten rows.
+ *                masks their unwritten rows, and the attention kernels never read them.
  *   seq_len      keys visible after the prefill tokens are written (= q_start + q_len)
  *   q_start      Delta of the query segment (= total document length)
  *   doc_blocks   number of document blocks (the query segment starts at this block)

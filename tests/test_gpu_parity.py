@@ -382,8 +382,9 @@ def test_sharpened_queries_separate_negative_controls(lk):
 
 # ------------------------------------------------------------------ poisoned caches
 POISON_CASES = {  # name -> (workload, requests checked, decode steps, steps checked)
-    # 32-token queries of a 4-head group: one live Q tile per CTA; 200-token documents end mid-page
-    "rag8b_one_q_tile": (lambda: make_workload("rag8b", batch=4), [0, 3], 2, {1}),
+    # 32-token queries of a 4-head group: one live Q tile per CTA; 200-token documents end
+    # mid-page; 16 requests x 8 head groups = 128 units: the decode's 12-warp CTAs
+    "rag8b_one_q_tile": (lambda: make_workload("rag8b"), [0, 3, 15], 2, {1}),
     # longer ragged queries: two live Q tiles per CTA, a partial second tile, documents of 1..1000
     "two_q_tiles": (lambda: make_custom([200, 37, 1000, 15, 1], [[0, 1, 2], [3, 4, 0], [2]], 8, 2, 128,
                                         PosCfg("rope", 5e5, 128), [70, 33, 100], 2, seed=77), [0, 1, 2], 2, {1}),
