@@ -171,16 +171,25 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_hash(text: str) -> str:
+    """sha256 (16 hex digits) of a C++/CUDA source with its comments and blank space removed:
+    it changes when the code changes, not when a comment does."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.strip() for ln in text.split("\n") if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def profiled_traffic(kernel_src: str, name: str):
     """Per-launch DRAM bytes recorded by an ncu capture in profiles/<name>, valid only while
-    the kernel source still hashes to the value recorded there."""
+    the kernel's code (comments aside) still hashes to the value recorded there."""
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
-    with open(os.path.join(ROOT, "position_agnostic_kv_gb300", "csrc", kernel_src), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(os.path.join(ROOT, "position_agnostic_kv_gb300", "csrc", kernel_src)) as f:
+        h = code_hash(f.read())
     text = open(path).read()
-    m_h = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_h = re.search(r"code_sha256_16:\s*([0-9a-f]{16})", text)
     m_t = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
     if not m_h or not m_t or m_h.group(1) != h:
         return None

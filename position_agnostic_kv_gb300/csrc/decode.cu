@@ -7,9 +7,11 @@
 // traffic stays that of plain paged attention (K and V only).
 //
 // Design (GB300):
-//  * One CTA = (query row, head group, KV split); 4 warps, each streaming a contiguous run of
-//    pages through its own 2-stage ring of shared-memory stages filled by cp.async.bulk (one
-//    4 KB K copy and one V copy per page and head, completed on an mbarrier); 3 CTAs per SM.
+//  * One CTA = (query row, head group, KV split); 4 warps (3 CTAs per SM), or 12 warps (one CTA
+//    per SM, no split) when a small batch's units fill between half and all of the SMs.  Each
+//    warp streams a contiguous run of pages through its own 2-stage ring of shared-memory
+//    stages filled by cp.async.bulk (one 4 KB K copy and one V copy per page and head,
+//    completed on an mbarrier).
 //    No registers are spent on loads in flight, and every stage is in flight while earlier
 //    pages are used.
 //  * A lane owns 8 columns (one 16-byte chunk) of a K/V row; D/8 lanes cover a row.  Per page

@@ -15,11 +15,13 @@
 //              online softmax in base 2 (the running max moves, and O is rescaled in TMEM, only
 //              when a row's max grows by more than 8), P written back to TMEM over S as bf16.
 //   warps 8-11 K rotation: each staged K tile's page rows rotated by their page's Delta in
-//              place in shared memory (cos/sin rows only per distinct Delta, double-buffered,
-//              reused while consecutive tiles stay inside one document).
+//              place in shared memory; a thread owns one chunk pair (8 frequencies) of 8 rows of
+//              a page and keeps their cos/sin in registers, recomputed when the Delta changes.
 //   warp 12    producer: unpacks the 64-bit block words of a tile's 8 pages (prefetched one tile
 //              ahead) and issues TMA loads (box 64 columns x 16 rows of one page, 128-byte
-//              swizzle) into 2-stage K and V rings.  A page with r < 16 rows that hold a key
+//              swizzle) into a 3-stage K ring (K runs two tiles ahead of V) and a 2-stage V
+//              ring; in the SPLIT_V instantiation warp 14 issues V with its own barrier chain
+//              (one live Q tile, long key ranges).  A page with r < 16 rows that hold a key
 //              visible to the CTA (a document's partial last page, or query-segment rows past
 //              the CTA's last token) is loaded from row r - 16: its r key rows land in the
 //              stage's last r rows and the 16 - r rows before them are out of the tensor's
@@ -40,6 +42,7 @@
 // key range is split over several CTAs and their partials are merged by log-sum-exp.
 // With ALiBi the tiles are visited newest first (the running max is fixed by the first tile).
 // Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
+// Warp 15 has no role, nor has warp 14 outside SPLIT_V (or warps 4-7 with one live Q tile).
 #include <cfloat>
 #include <climits>
 
@@ -106,7 +109,7 @@ struct Layout {
   static constexpr int PSTART_OFF = V_OFF + kVStages * TILE;  // int [slot][8] key position of stage row 0
   static constexpr int PINFO_OFF = PSTART_OFF + kSlots * kPagesPerTile * 4;  // int2 [slot][8] {Delta, lo}:
                                                                             // stage rows [lo, 16) hold keys
-  static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, unused}
+  static constexpr int FLAG_OFF = PINFO_OFF + kSlots * kPagesPerTile * 8;  // int [slot][2] {fast, pad}
   static constexpr int PGID_OFF = FLAG_OFF + kSlots * 8;                // int [slot][8] page * Hkv + head
   static constexpr int TURNS_OFF = PGID_OFF + kSlots * kPagesPerTile * 4;  // u64 [D/2]
   static constexpr int BAR_OFF = TURNS_OFF + (D / 2) * 8;
