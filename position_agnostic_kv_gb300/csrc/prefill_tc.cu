@@ -854,7 +854,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       };
       uint64_t w_next = fetch(0);
       int issued_v = 0;
-      for (int j = 0; j < ntiles; ++j) {
+      // With rotation, V waits until Q is ready (V is first needed by PV(0), after QK(0) and its
+      // softmax): the K chain, whose tiles must also be rotated, has the copy engine to itself
+      // while the Q rows are prepared.  Measured: 322 -> 308 us on a 32-request, 12 000-key
+      // YaRN prefill, and slower for the ALiBi decode, which keeps the early V copies.
+      int ntiles_v = ntiles;
+      if constexpr (kRotate) {
+        const bool q_ready = wait_bar(BAR(B_Q_READY), 0, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, q_ready)) ntiles_v = 0;
+      }
+      for (int j = 0; j < ntiles_v; ++j) {
         const int s = j % kVStages;
         const uint64_t w = w_next;
         w_next = fetch(j + 1);

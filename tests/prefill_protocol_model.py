@@ -53,17 +53,18 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3, vprod=False):
+    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3, vprod=False, vgate=True):
         """ntiles K/V tiles, nq live Q tiles (1 or 2), `clean(j)`: whether tile j has key-less
         rows (used only by subclasses that model a V-cleaning role); kst K ring stages (the V
         ring has 2); slots metadata slots; vprod: V is issued by a producer of its own, which
-        reads the block words itself (no metadata slot)."""
+        reads the block words itself (no metadata slot); vgate: that producer first waits for
+        Q_READY (the rotating kernels)."""
         self.rng = random.Random(seed)
         self.now = 0
         self.max_latency = self.rng.choice([0, 3, 12, 40])
         self.n, self.nq = ntiles, nq
         self.clean_of = clean or (lambda j: False)
-        self.slots, self.kst, self.vprod = slots, kst, vprod
+        self.slots, self.kst, self.vprod, self.vgate = slots, kst, vprod, vgate
         self.K_FULL = [Bar(f"K_FULL{s}", 1) for s in range(kst)]
         self.K_READY = [Bar(f"K_READY{s}", 1) for s in range(kst)]
         self.K_FREE = [Bar(f"K_FREE{s}", 1) for s in range(kst)]
@@ -201,6 +202,8 @@ class Sim:
         yield ("step",)
 
     def vproducer(self):
+        if self.vgate:  # the rotating kernels' V producer starts once Q is ready
+            yield ("wait", self.Q_READY, 0)
         for j in range(self.n):
             yield from self.issue_v(j, from_slot=False)
 

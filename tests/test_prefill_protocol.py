@@ -52,10 +52,11 @@ def test_separate_v_producer_is_safe_for_both_schedules():
     """V issued by a warp of its own that reads the block words itself: the SPLIT_V
     instantiation (one-Q-tile CTAs over long key ranges); safe for both schedules."""
     for seed, n, nq, clean in _schedules(300, seed0=9000):
-        try:
-            pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=3, slots=6, vprod=True).run()
-        except pm.ProtocolError as e:
-            pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles: {e}")
+        for vgate in (True, False):  # rotating kernels: V starts once Q is ready; the others at once
+            try:
+                pm.Sim(n, nq, CLEAN[clean], seed=seed, kst=3, slots=6, vprod=True, vgate=vgate).run()
+            except pm.ProtocolError as e:
+                pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles, vgate {vgate}: {e}")
 
 
 def test_two_stage_k_ring_is_safe_too():
