@@ -121,9 +121,9 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4 && G <= 4) ? 3 : 1) decode_k
   const int chunk = (nb + a.S - 1) / a.S;
   const int beg = split * chunk, end = min(nb, beg + chunk);
   const int len = max(0, end - beg);
-  const int wch = (len + NW - 1) / NW;
-  const int wb = beg + warp * wch;
-  const int n = max(0, min(end, wb + wch) - wb);
+  // the warps' runs differ by at most one page
+  const int wb = beg + warp * len / NW;
+  const int n = beg + (warp + 1) * len / NW - wb;
 
   float* qs = reinterpret_cast<float*>(smem + L::QS_OFF);
   float* pbuf = reinterpret_cast<float*>(smem + L::PB_OFF) + warp * kPage * G;
@@ -131,18 +131,24 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4 && G <= 4) ? 3 : 1) decode_k
   const uint32_t bar0 = smem_u32(smem + L::BAR_OFF + warp * NST * 8);
   const uint32_t stage0 = smem_u32(smem + warp * NST * L::STAGE_BYTES);
 
-  // ---- block words of this warp's run, 32 at a time (coalesced), next chunk prefetched; issued
-  // before the query loads so that the two latencies overlap
+  // ---- block words of this warp's run, 32 at a time (coalesced), next chunk prefetched, and the
+  // query values loaded into registers, so that the two latencies overlap; the first pages are
+  // issued as soon as the block words arrive, before the query is staged in shared memory
   const uint64_t* mrow = a.meta + (size_t)b * a.max_blocks + wb;
   uint64_t mcur = lane < n ? ldg_u64(mrow + lane) : 0;
   uint64_t mnxt = 32 + lane < n ? ldg_u64(mrow + 32 + lane) : 0;
   int mbase = 0;
-
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = __bfloat162float(qrow[h0 * D + i]);
+  constexpr int QPT = (G * D + NW * 32 - 1) / (NW * 32);  // query values per thread
+  __nv_bfloat16 qv[QPT];
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = threadIdx.x + k * NW * 32;
+    qv[k] = i < G * D ? qrow[h0 * D + i] : __float2bfloat16_rn(0.f);
+  }
   if (lane == 0)
     for (int s = 0; s < NST; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
-  __syncthreads();
+  __syncwarp();
 
   const size_t head_stride = (size_t)kPage * D;  // elements per (page, head)
   auto issue = [&](int i) {
@@ -178,6 +184,12 @@ __global__ void __launch_bounds__(NW * 32, (NW == 4 && G <= 4) ? 3 : 1) decode_k
 
   const int pre = min(NST, n);
   for (int i = 0; i < pre; ++i) issue(i);
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = threadIdx.x + k * NW * 32;
+    if (i < G * D) qs[i] = __bfloat162float(qv[k]);
+  }
+  __syncthreads();  // qs complete
 
   // ---- per-lane state
   const int c = lane % LPR;        // chunk (8 columns) of this lane
