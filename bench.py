@@ -354,12 +354,14 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
     hbm_peak = float(peaks["hbm_gbs"])
     achieved_gbs = avg_dec_bytes / (avg_dec_ms / 1e3) / 1e9 if dec_ms else None
     pre_flops = prefill_flops(w, pb)
+    # mean over the timed steps (single launches jitter in ~2 us steps; see rotation_overhead)
     pre_med = statistics.median(pre_ms) if pre_ms else None
-    pre_tflops = pre_flops / (pre_med / 1e3) / 1e12 if pre_med else None
+    pre_mean = statistics.fmean(pre_ms) if pre_ms else None
+    pre_tflops = pre_flops / (pre_mean / 1e3) / 1e12 if pre_mean else None
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     dec_total = avg_dec_ms * n_dec if dec_ms else 0.0
-    if dec_total >= (pre_med or 0.0):  # the dominant kernel of the step
+    if dec_total >= (pre_mean or 0.0):  # the dominant kernel of the step
         traffic = profiled_traffic("decode.cu", f"decode_{name}_{sharing}.md")
         roofline = {"kernel": "lazy_attn_decode (split-KV decode + lse merge)", "bound": "hbm",
                     "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -371,7 +373,7 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
         roofline = {"kernel": "lazy_attn_prefill (tcgen05)", "bound": "tensor", "achieved": pre_tflops,
                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": pre_tflops / bf16_peak,
                     "peak_source": f"{peak_kind} bf16_tflops (burst)", "traffic": traffic,
-                    "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_med * 1e3}
+                    "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_mean * 1e3}
     res = {
         "value": value, "ms_per_step": mean_ms, "tokens_per_step": tokens_per_step,
         "workload": f"{name}: {WORKLOAD_TEXT[name]}" + (f" (first {w.B} requests)" if w.B != make_workload(
@@ -387,6 +389,7 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
             "launches_per_step": n_dec},
         "step_prefill": None if pre is None else {
             "kernel": "lazy_attn_prefill", "flops_per_launch": pre_flops,
+            "mean_us": pre_mean * 1e3 if pre_mean else None,
             "median_us": pre_med * 1e3 if pre_med else None, "tflops": pre_tflops,
             "frac_bf16_peak": pre_tflops / bf16_peak if pre_tflops else None,
             "hbm_bytes_per_launch": prefill_bytes(w, pb),
@@ -442,10 +445,11 @@ def prefill_probe(args, dist, lk, name, sharing):
     tflops = flops / (us / 1e6) / 1e12
     return {"workload": f"{name}: {WORKLOAD_TEXT[name]}", "sharing": sharing,
             "kernel": "lazy_attn_prefill (tcgen05)", "flops_per_launch": flops,
-            "hbm_bytes_per_launch": prefill_bytes(w, pb), "median_us": us, "tflops": tflops,
+            "hbm_bytes_per_launch": prefill_bytes(w, pb), "mean_us": us,
+            "median_us": ovh["prefill"]["median_us"]["rot"], "tflops": tflops,
             "frac_bf16_peak": tflops / bf16_peak, "peak": bf16_peak,
             "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed on its own)",
-            "timing": "eager launches, L2 flushed before each, median (same runs as rotation_overhead)",
+            "timing": "eager launches, L2 flushed before each, mean (same runs as rotation_overhead)",
             "traffic": profiled_traffic("prefill_tc.cu", f"prefill_{name}_{sharing}.md"),
             "rotation_overhead": ovh["prefill"] | {"method": ovh["method"],
                                                    **({"launch_errors": ovh["launch_errors"]}
@@ -504,8 +508,10 @@ def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
     """Deferred-rotation cost: the same attention launches over the same caches with
     (rot) the workload's rotary kind, (delta0) the kernels built without any positional work
     (the Delta = 0 twin), and (same_delta) the rotary kernels with every block's Delta set to 0,
-    so that no document boundary occurs.  Eager launches, L2 flushed before each, median of
-    the repetitions; overhead = t_rot / t_delta0 - 1."""
+    so that no document boundary occurs.  Eager launches, L2 flushed before each; each time is
+    the mean of the repetitions (a single launch takes one of a few values about 2 us apart,
+    start-up jitter of the GPU, so a median snaps to one of them while the mean weighs them;
+    the medians are reported too); overhead = t_rot / t_delta0 - 1."""
     import numpy as np
     import torch
     cfg_none = lk.pos_cfg_from("none", pb.D)
@@ -519,7 +525,7 @@ def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
     for phase in ("prefill", "decode"):
         if (phase == "prefill" and pre is None) or (phase == "decode" and not decs):
             continue
-        med = {}
+        med, mean = {}, {}
         for name, (cfg, meta) in variants.items():
             ts = []
             for r in range(reps + 2):
@@ -544,12 +550,14 @@ def rotation_overhead(args, lk, pb, pre, decs, out_p, outs_d, stream, flush):
                     elif r >= 2:
                         ts.append(e0.elapsed_time(e1) * 1e3)
             med[name] = statistics.median(ts) if ts else float("nan")
-        out[phase] = {"rot_us": med["rot"], "delta0_us": med["delta0"], "same_delta_us": med["same_delta"],
-                      "overhead": med["rot"] / med["delta0"] - 1.0,
-                      "boundary_share": (med["rot"] - med["same_delta"]) / med["delta0"]}
+            mean[name] = statistics.fmean(ts) if ts else float("nan")
+        out[phase] = {"rot_us": mean["rot"], "delta0_us": mean["delta0"], "same_delta_us": mean["same_delta"],
+                      "overhead": mean["rot"] / mean["delta0"] - 1.0,
+                      "boundary_share": (mean["rot"] - mean["same_delta"]) / mean["delta0"],
+                      "median_us": {"rot": med["rot"], "delta0": med["delta0"], "same_delta": med["same_delta"]}}
     out["method"] = ("same caches and inputs; rot = rotary kind of the workload, delta0 = kernels "
                      "without positional work, same_delta = rotary kernels with every Delta = 0; "
-                     f"eager launches, L2 flushed before each, median of {reps} reps"
+                     f"eager launches, L2 flushed before each, mean of {reps} reps (medians alongside)"
                      + (f", decode steps {dec_idx}" if decs else ""))
     if errors:  # reported, not hidden: launches whose kernels set a device status bit
         out["launch_errors"] = {"count": errors, "status_bits": sorted(hex(x) for x in statuses)}
