@@ -36,13 +36,19 @@
 //              commit that signals S_i(j+1) also covers PV_i(j).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i = first 64 of S_i.
 // With one live Q tile (short queries, decode), S0 and S1 double-buffer that tile's scores
-// instead (tile j in S_{j%2}), so QK^T of tile j+1 runs while the softmax works on tile j.
+// instead (tile j in S_{j%2}), so QK^T of tile j+1 runs while the softmax works on tile j.  In
+// launches whose CTAs all have one live Q tile (the KH instantiation) warps 0-3 and 4-7 each
+// take half of every tile's keys (keys 0-63 / 64-127, P over the start of each half's own S
+// columns): two partial softmaxes accumulated into O_A [256,384) and O_B [384,512) by two PV
+// MMAs of 64 keys, merged by their maxima and sums in the epilogue.  A softmax warp thus does
+// half the work per tile, and each SM sub-partition has two of them.
 // GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
 // Decode mode serves wide head groups (MQA): the G heads of one new token fill the rows, the
 // key range is split over several CTAs and their partials are merged by log-sum-exp.
 // With ALiBi the tiles are visited newest first (the running max is fixed by the first tile).
 // Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
-// Warp 15 has no role, nor has warp 14 outside SPLIT_V (or warps 4-7 with one live Q tile).
+// Warp 15 has no role, nor has warp 14 outside SPLIT_V (or warps 4-7 of a CTA with one live
+// Q tile outside KH).
 #include <cfloat>
 #include <climits>
 
@@ -270,7 +276,7 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the MUFU (approx, flu
 // (decode mode, long-context prefill with short queries), where V copies queued behind K leave
 // the ingest short; the two-Q-tile schedule keeps one producer.  A separate instantiation, so
 // each schedule's code is generated on its own.
-template <int D, int POS, bool SPLIT_V>
+template <int D, int POS, bool SPLIT_V, bool KH>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Args a) {
   using L = Layout<D>;
@@ -339,7 +345,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     }
     for (int i = 0; i < kQT; ++i) {
       mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_P_FULL + i), 128);
+      mbar_init(BAR(B_P_FULL + i), KH ? 256 : 128);  // key halves: both warpgroups write P
     }
     mbar_init(BAR(B_Q_READY), 2 * 128);
     mbar_init(BAR(B_FINAL), 1);
@@ -362,13 +368,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
   if (warp < 2 * 4) {
     // ============================ Q preparation, softmax and epilogue of Q tile qt
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::softmax));
+    // qt: the warpgroup's Q tile, or (KH) its half of the keys of the one Q tile
     const int qt = warp >> 2;
     const int r = threadIdx.x & (kM - 1);  // row of the tile = TMEM lane
-    const int token = tok0 + qt * tpt + r / G;
+    const int token = tok0 + (KH ? 0 : qt * tpt) + r / G;
     const int h = g * G + r % G;
     const bool valid = token < Lq;
     const int m_row = valid ? mbase + token : -1;
-    {
+    if (KH && qt == 1) {
+      mbar_arrive(BAR(B_Q_READY));  // one Q tile, prepared by the first warpgroup
+    } else {
       const uint32_t sQ = sQ0 + uint32_t(qt * L::QTILE);
       // The raw row is staged in this thread's own row of the Q tile (bf16, swizzled), then
       // rotated and scaled chunk by chunk in place, so a rotation partner at a run-time offset
@@ -446,7 +455,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       fence_async_smem();
       mbar_arrive(BAR(B_Q_READY));
     }
-    if (qt < nq) {
+    if (KH || qt < nq) {
       float slope = 0.f;
       if constexpr (POS == kAlibi) slope = a.pos.slopes[h] * 1.4426950408889634f;
       const uint32_t tl = tmem + (uint32_t(32 * (warp & 3)) << 16);
@@ -462,26 +471,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
         tc_fence_after();
         const bool fast = flags[slot * 2] != 0;  // every key of the tile is visible to every row
-        // the whole S row in registers: four loads, one wait
-        uint32_t v[kN];
-        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-        tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+        // this thread's scores in registers (the whole row, or with key halves its warpgroup's
+        // 64 keys = page slots pg0 .. pg0 + 3): loads, one wait
+        constexpr int NK = KH ? kN / 2 : kN, NPG = NK / kPage;
+        const int pg0 = KH ? NPG * qt : 0;
+        uint32_t v[NK];
+#pragma unroll
+        for (int c = 0; c < NK / 32; ++c)
+          tmem_ld32(tS + uint32_t(pg0 * kPage + 32 * c), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
         tmem_wait_ld();
         if (POS == kAlibi && fast) {  // bias only: -slope (m - p), p = start + t
 #pragma unroll
-          for (int pp = 0; pp < kPagesPerTile; ++pp) {
-            const float base = slope * float(pstart[slot * kPagesPerTile + pp] - m_row);
+          for (int pp = 0; pp < NPG; ++pp) {
+            const float base = slope * float(pstart[slot * kPagesPerTile + pg0 + pp] - m_row);
 #pragma unroll
             for (int t = 0; t < kPage; ++t)
               v[pp * kPage + t] = __float_as_uint(__uint_as_float(v[pp * kPage + t]) + fmaf(slope, float(t), base));
           }
         } else if (!fast) {  // stage row t of a page holds key p = pstart + t; visible iff t >= lo, p <= m
 #pragma unroll
-          for (int pp = 0; pp < kPagesPerTile; ++pp) {
-            const int st = pstart[slot * kPagesPerTile + pp];
-            const int lo = pinfo[slot * kPagesPerTile + pp].y;
+          for (int pp = 0; pp < NPG; ++pp) {
+            const int st = pstart[slot * kPagesPerTile + pg0 + pp];
+            const int lo = pinfo[slot * kPagesPerTile + pg0 + pp].y;
             const int hi = m_row - st + 1;
             float base = 0.f;
             if constexpr (POS == kAlibi) base = slope * float(st - m_row);
@@ -493,17 +504,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             }
           }
         }
-        // row max over 128 scores: eight independent runs of three-input maxima, then a tree
-        float mq[8];
+        // row max over the scores: independent runs of three-input maxima over 16, then a tree
+        float mq[NK / 16];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < NK / 16; ++q) {
           const float* x = reinterpret_cast<const float*>(v + 16 * q);
           float m = max3f(x[0], x[1], x[2]);
 #pragma unroll
           for (int e = 3; e < 15; e += 2) m = max3f(m, x[e], x[e + 1]);
           mq[q] = fmaxf(m, x[15]);
         }
-        const float mx = max3f(max3f(mq[0], mq[1], mq[2]), max3f(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
+        float mx;
+        if constexpr (KH)
+          mx = max3f(max3f(mq[0], mq[1], mq[2]), mq[3], mq[3]);
+        else
+          mx = max3f(max3f(mq[0], mq[1], mq[2]), max3f(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
         const bool need = mx > m_run + kTau;
         const float m_new = need ? mx : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
@@ -512,7 +527,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
                           make_float2(0.f, 0.f)};  // four independent partial sums
         // P packed to bf16 pairs in place: pair e (keys 2e, 2e+1) lands in v[e] (already consumed)
 #pragma unroll
-        for (int e = 0; e < kN / 2; ++e) {
+        for (int e = 0; e < NK / 2; ++e) {
           float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
           x = __fadd2_rn(x, mneg);
           const float2 ev = make_float2(ex2(x.x), ex2(x.y));
@@ -543,15 +558,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
           }
         }
         m_run = m_new;
-        // P row -> TMEM over the first 64 columns of S (column e holds keys 2e, 2e+1)
-        tmem_st32(tS + 0, *reinterpret_cast<const uint32_t(*)[32]>(v + 0));
-        tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
+        // P row -> TMEM over the first 64 columns of S (column e holds keys 2e, 2e+1); with key
+        // halves each warpgroup writes its 32 columns over the start of its own S columns
+        // (keys 64h .. 64h + 63 -> columns 64h .. 64h + 31), never over the other's scores
+#pragma unroll
+        for (int c = 0; c < NK / 64; ++c)
+          tmem_st32(tS + uint32_t(pg0 * kPage + 32 * c), *reinterpret_cast<const uint32_t(*)[32]>(v + 32 * c));
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(BAR(B_P_FULL + buf));
       }
       const bool got_last = ok && wait_bar(BAR(B_FINAL), 0, abort_flag, a.status);
-      if (__all_sync(0xffffffffu, got_last) && a.S > 1) {
+      if constexpr (KH) {
+        // The two key halves of a row are two partial softmaxes (O_A over keys 0-63 of every
+        // tile, O_B over keys 64-127): merged by their maxima and sums, exchanged through the
+        // unused second Q tile's space.  Each warpgroup writes its 64 output columns.
+        float2* xml = reinterpret_cast<float2*>(sm + L::Q_OFF + L::QTILE);
+        xml[qt * kM + r] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
+        named_sync(1, 2 * kM);  // the two softmax warpgroups
+        const float2 mine = xml[qt * kM + r], other = xml[(qt ^ 1) * kM + r];
+        const float2 hA = qt == 0 ? mine : other, hB = qt == 0 ? other : mine;
+        const float M = fmaxf(hA.x, hB.x);
+        const float wA = hA.y > 0.f ? ex2(hA.x - M) : 0.f, wB = hB.y > 0.f ? ex2(hB.x - M) : 0.f;
+        const float Lt = wA * hA.y + wB * hB.y;
+        if (__all_sync(0xffffffffu, got_last)) {
+          tc_fence_after();
+          const bool part = a.S > 1;
+          const float inv = part ? 1.f : (Lt > 0.f ? 1.f / Lt : 0.f);
+          const size_t pi = ((size_t)(q0 + token) * a.Hq + h) * a.S + split;
+          __nv_bfloat16* orow = a.out + ((size_t)(q0 + token) * a.Hq + h) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            const int col = qt * (D / 2) + c * 32;
+            uint32_t oa[32], ob[32];
+            tmem_ld32(tl + uint32_t(2 * kN + col), oa);
+            tmem_ld32(tl + uint32_t(3 * kN + col), ob);
+            tmem_wait_ld();
+            float o[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = (wA * __uint_as_float(oa[e]) + wB * __uint_as_float(ob[e])) * inv;
+            if (valid && part) {
+              float4* dst = reinterpret_cast<float4*>(a.part_o + pi * D + col);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) dst[q4] = make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+            } else if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_uint4(f2_to_bf2(o[8 * q4], o[8 * q4 + 1]), f2_to_bf2(o[8 * q4 + 2], o[8 * q4 + 3]),
+                                     f2_to_bf2(o[8 * q4 + 4], o[8 * q4 + 5]), f2_to_bf2(o[8 * q4 + 6], o[8 * q4 + 7]));
+            }
+          }
+          if (valid && qt == 0) {
+            if (part) {
+              a.part_ml[pi * 2] = Lt > 0.f ? M : -INFINITY;
+              a.part_ml[pi * 2 + 1] = Lt;
+            } else if (a.lse) {
+              a.lse[(size_t)(q0 + token) * a.Hq + h] = (M + log2f(Lt)) * 0.6931471805599453f;
+            }
+          }
+        }
+      } else if (__all_sync(0xffffffffu, got_last) && a.S > 1) {
         tc_fence_after();
         const size_t pi = ((size_t)(q0 + token) * a.Hq + h) * a.S + split;
 #pragma unroll 1
@@ -966,9 +1033,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
             tc_fence_after();
             const uint32_t sV = sV0 + uint32_t((j % kVStages) * L::TILE);
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              mma_ts(tmem + uint32_t(2 * kN), tmem + uint32_t((j & 1) * kN + kk * 8),
-                     sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024), IPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk) {
+              // key halves: keys 0-63 into O_A (columns 2 kN), keys 64-127 into O_B (3 kN), each
+              // half's P at the start of its own S columns
+              const int hk = KH ? kk / 4 : 0;
+              const uint32_t pcol = uint32_t((j & 1) * kN + (KH ? 64 * hk + (kk % 4) * 8 : kk * 8));
+              mma_ts(tmem + uint32_t((2 + hk) * kN), tmem + pcol, sdesc(sV + uint32_t(kk * 16 * 128), L::BLK, 1024),
+                     IPV, (j > 0 || kk > (KH ? 4 * hk : 0)) ? 1u : 0u);
+            }
             mma_commit(BAR(B_PV_DONE));
             mma_commit(BAR(B_V_FREE + j % kVStages));
             if (j + 2 < ntiles) ok = qk1(j + 2);
@@ -1083,11 +1155,11 @@ static int cache_map(CUtensorMap* map, const void* base, int num_pages, int Hkv,
   return LAZY_OK;
 }
 
-template <int D, int POS, bool SPLIT_V>
+template <int D, int POS, bool SPLIT_V, bool KH>
 static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q, cudaStream_t st) {
   // (decode mode: max_q = 1, one query row per request)
   using L = tc::Layout<D>;
-  auto kern = tc::prefill_tc_kernel<D, POS, SPLIT_V>;
+  auto kern = tc::prefill_tc_kernel<D, POS, SPLIT_V, KH>;
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1114,19 +1186,19 @@ static int launch_tc(const CUtensorMap& mk, const CUtensorMap& mv, const tc::Arg
   return LAZY_OK;
 }
 
-template <bool SPLIT_V>
+template <bool SPLIT_V, bool KH>
 static int dispatch_tc(int D, int kind, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Args& a, int max_q,
                        cudaStream_t st) {
   if (D == 128) {
-    if (kind == kRope) return launch_tc<128, kRope, SPLIT_V>(mk, mv, a, max_q, st);
-    if (kind == kRopeX) return launch_tc<128, kRopeX, SPLIT_V>(mk, mv, a, max_q, st);
-    if (kind == kAlibi) return launch_tc<128, kAlibi, SPLIT_V>(mk, mv, a, max_q, st);
-    return launch_tc<128, kNone, SPLIT_V>(mk, mv, a, max_q, st);
+    if (kind == kRope) return launch_tc<128, kRope, SPLIT_V, KH>(mk, mv, a, max_q, st);
+    if (kind == kRopeX) return launch_tc<128, kRopeX, SPLIT_V, KH>(mk, mv, a, max_q, st);
+    if (kind == kAlibi) return launch_tc<128, kAlibi, SPLIT_V, KH>(mk, mv, a, max_q, st);
+    return launch_tc<128, kNone, SPLIT_V, KH>(mk, mv, a, max_q, st);
   }
-  if (kind == kRope) return launch_tc<64, kRope, SPLIT_V>(mk, mv, a, max_q, st);
-  if (kind == kRopeX) return launch_tc<64, kRopeX, SPLIT_V>(mk, mv, a, max_q, st);
-  if (kind == kAlibi) return launch_tc<64, kAlibi, SPLIT_V>(mk, mv, a, max_q, st);
-  return launch_tc<64, kNone, SPLIT_V>(mk, mv, a, max_q, st);
+  if (kind == kRope) return launch_tc<64, kRope, SPLIT_V, KH>(mk, mv, a, max_q, st);
+  if (kind == kRopeX) return launch_tc<64, kRopeX, SPLIT_V, KH>(mk, mv, a, max_q, st);
+  if (kind == kAlibi) return launch_tc<64, kAlibi, SPLIT_V, KH>(mk, mv, a, max_q, st);
+  return launch_tc<64, kNone, SPLIT_V, KH>(mk, mv, a, max_q, st);
 }
 
 int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, const int32_t* doc_blocks,
@@ -1170,9 +1242,12 @@ int run_prefill_tc(const void* q, const int32_t* cu_q, const int32_t* q_start, c
   // A/B): MQA decode 53.2 -> 49.6 us, yarn8b prefill 340 -> 323-330 us; rag8b's 16-tile CTAs
   // were slower with it.
   const int tiles_per_cta = ((max_blocks + tc::kPagesPerTile - 1) / tc::kPagesPerTile + S - 1) / S;
-  const bool split_v = (seq_len != nullptr || max_q <= tc::kM / G) && tiles_per_cta >= 20;
-  if (split_v) return dispatch_tc<true>(D, kind, mk, mv, a, max_q, st);
-  return dispatch_tc<false>(D, kind, mk, mv, a, max_q, st);
+  const bool one_tile = seq_len != nullptr || max_q <= tc::kM / G;  // one live Q tile in every CTA
+  const bool split_v = one_tile && tiles_per_cta >= 20;
+  // With one live Q tile the second softmax warpgroup takes half of every tile's keys (KH).
+  if (split_v) return dispatch_tc<true, true>(D, kind, mk, mv, a, max_q, st);
+  if (one_tile) return dispatch_tc<false, true>(D, kind, mk, mv, a, max_q, st);
+  return dispatch_tc<false, false>(D, kind, mk, mv, a, max_q, st);
 }
 
 }  // namespace lazykv

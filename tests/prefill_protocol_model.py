@@ -53,12 +53,13 @@ class Bar:
 
 
 class Sim:
-    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3, vprod=False, vgate=True):
+    def __init__(self, ntiles, nq, clean=None, seed=0, slots=4, kst=3, vprod=False, vgate=True, kh=False):
         """ntiles K/V tiles, nq live Q tiles (1 or 2), `clean(j)`: whether tile j has key-less
         rows (used only by subclasses that model a V-cleaning role); kst K ring stages (the V
         ring has 2); slots metadata slots; vprod: V is issued by a producer of its own, which
         reads the block words itself (no metadata slot); vgate: that producer first waits for
-        Q_READY (the rotating kernels)."""
+        Q_READY (the rotating kernels); kh: with one live Q tile the two softmax roles each take
+        half of every tile's keys."""
         self.rng = random.Random(seed)
         self.now = 0
         self.max_latency = self.rng.choice([0, 3, 12, 40])
@@ -71,7 +72,10 @@ class Sim:
         self.V_FULL = [Bar(f"V_FULL{s}", 1) for s in range(2)]
         self.V_FREE = [Bar(f"V_FREE{s}", 1) for s in range(2)]
         self.S_FULL = [Bar(f"S_FULL{i}", 1) for i in range(2)]
-        self.P_FULL = [Bar(f"P_FULL{i}", 1) for i in range(2)]
+        # kh (one live Q tile): both softmax roles work on every tile, each on half of its keys,
+        # and P is complete once both have written theirs
+        self.kh = kh and nq == 1
+        self.P_FULL = [Bar(f"P_FULL{i}", 2 if self.kh else 1) for i in range(2)]
         self.PV_DONE = Bar("PV_DONE", 1)
         self.Q_READY = Bar("Q_READY", 2)
         self.FINAL = Bar("FINAL", 1)
@@ -141,7 +145,7 @@ class Sim:
             prev = self.s_buf.get(buf)
             if prev is not None and prev[0] == "P" and (i, prev[1]) not in self.done_pv:
                 raise ProtocolError(f"QK{i}({j}) overwrites P({prev[1]}) in S{buf} before its PV")
-            if prev is not None and prev[0] == "S":
+            if prev is not None and prev[0] in ("S", "P1"):
                 raise ProtocolError(f"QK{i}({j}) overwrites S({prev[1]}) in S{buf} before the softmax read it")
             if (i, j) in self.done_qk:
                 raise ProtocolError(f"QK{i}({j}) runs twice")
@@ -220,21 +224,24 @@ class Sim:
 
     def softmax(self, i):
         self.Q_READY.arrive()
-        if i >= self.nq:
+        if i >= self.nq and not self.kh:
             return
         yield ("step",)
         for j in range(self.n):
             buf = i if self.nq == 2 else (j & 1)
             e = j if self.nq == 2 else (j >> 1)
             yield ("wait", self.S_FULL[buf], e)
-            if self.s_buf.get(buf) != ("S", j):
+            if self.s_buf.get(buf) not in (("S", j), ("P1", j)):  # P1: the other half's P is in
                 raise ProtocolError(f"softmax{i} reads S{buf} for tile {j}, holds {self.s_buf.get(buf)}")
             self.read_slot(j, f"softmax{i}")
             yield ("step",)
             if self.nq == 1 and j > 0:
                 yield ("wait", self.PV_DONE, j - 1)
             self.read_slot(j, f"softmax{i}-mask")
-            self.s_buf[buf] = ("P", j)
+            if self.kh and self.s_buf.get(buf) == ("S", j):
+                self.s_buf[buf] = ("P1", j)
+            else:
+                self.s_buf[buf] = ("P", j)
             self.P_FULL[buf].arrive()
         yield ("wait", self.FINAL, 0)
 

@@ -38,6 +38,31 @@ def test_protocol_as_built_is_safe_under_random_interleavings(part):
             pytest.fail(f"seed {seed}, {n} tiles, {nq} live Q tiles: {e}")
 
 
+def test_key_halves_with_one_live_q_tile_are_safe():
+    """Launches whose CTAs all have one live Q tile: the two softmax warpgroups each take half of
+    every tile's keys (P complete after both), with one producer or the separate V producer."""
+    for seed, n, _, clean in _schedules(600, seed0=5000):
+        for vprod in (False, True):
+            try:
+                pm.Sim(n, 1, CLEAN[clean], seed=seed, kst=3, slots=6, vprod=vprod, kh=True).run()
+            except pm.ProtocolError as e:
+                pytest.fail(f"seed {seed}, {n} tiles, separate V producer {vprod}: {e}")
+
+
+def test_model_catches_pv_after_one_key_half():
+    class OneHalfEnough(pm.Sim):
+        def __init__(self, *a, **kw):
+            super().__init__(*a, **kw)
+            self.P_FULL = [pm.Bar(f"P_FULL{i}", 1) for i in range(2)]  # planted: PV after one half
+    caught = []
+    for seed, n, _, clean in _schedules(300):
+        try:
+            OneHalfEnough(n, 1, CLEAN[clean], seed=seed, kst=3, slots=6, kh=True).run()
+        except pm.ProtocolError as e:
+            caught.append(str(e))
+    assert any("P1" in c or "too many arrivals" in c for c in caught), caught[:3]
+
+
 def _caught(make, n_runs=200):
     caught = 0
     for seed, n, nq, clean in _schedules(n_runs):
