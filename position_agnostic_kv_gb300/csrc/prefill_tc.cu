@@ -74,12 +74,16 @@ constexpr int kRotWarp0 = 8;
 constexpr int kProdWarp = 12;
 constexpr int kMmaWarp = 13;
 constexpr int kVProdWarp = 14;  // V producer of the SPLIT_V instantiation
-// Registers per thread after the re-split, per warpgroup role (the splits with no spills):
-// kernels that rotate K give the rotation warps more (2*128*184 + 128*56 + 128*88), the others
-// give the softmax more (2*128*192 + 128*48 + 128*80); both add up to 512 * 128 = 65536.
+// Registers per thread after the re-split, per warpgroup role (softmax, rotation, producer +
+// MMA), chosen by the spills ptxas reports: kernels that rotate K give the rotation warps 56
+// (48 spills there); two Q tiles keep a 128-score row per softmax thread (184 or 192), while
+// with key halves a softmax thread holds 64 scores and 176 leave the producer and MMA warps
+// enough to spill nothing.  Every split adds up to 512 * 128 = 65536.
 constexpr int kRegsLaunch = 128;
-template <bool ROT> struct Regs {
-  static constexpr int softmax = ROT ? 184 : 192, rot = ROT ? 56 : 48, issue = ROT ? 88 : 80;
+template <bool ROT, bool KH = false> struct Regs {
+  static constexpr int softmax = KH ? 176 : (ROT ? 184 : 192);
+  static constexpr int rot = ROT ? 56 : 48;
+  static constexpr int issue = KH ? (ROT ? 104 : 112) : (ROT ? 88 : 80);
   static_assert(2 * 128 * softmax + 128 * rot + 128 * issue == kThreads * kRegsLaunch,
                 "warpgroup register shares must add up to the launch allocation");
 };
@@ -367,7 +371,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
 
   if (warp < 2 * 4) {
     // ============================ Q preparation, softmax and epilogue of Q tile qt
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::softmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<kRotate, KH>::softmax));
     // qt: the warpgroup's Q tile, or (KH) its half of the keys of the one Q tile
     const int qt = warp >> 2;
     const int r = threadIdx.x & (kM - 1);  // row of the tile = TMEM lane
@@ -669,7 +673,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
     // barrier among the rotation threads.  Partial rotary_dim / interleaved pairs: each thread
     // owns one chunk task (a rotated chunk pair or chunk, or one unrotated chunk converted to
     // f16) for all 16 rows of its page.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::rot));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate, KH>::rot));
     const int rt = threadIdx.x - kRotWarp0 * 32;
     const int ps = rt / kPage, l = rt % kPage;
     constexpr int NCP = D / 16;  // chunk pairs per row (full width)
@@ -782,7 +786,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
       mbar_arrive(BAR(B_K_READY + s));
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate>::issue));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<kRotate, KH>::issue));
     if (warp == kProdWarp) {
       // ============================ block words + TMA
       // Issue order K0, K1, V0, K2, V1, ...: a K stage is refilled once both its QK^T are done, a
