@@ -380,6 +380,36 @@ def test_sharpened_queries_separate_negative_controls(lk):
         assert err > 2e-2, f"negative control not separated: {err:.3e}"
 
 
+# ------------------------------------------------------------------ log-sum-exp output
+@pytest.mark.parametrize("Hq,Hkv,q_len,path", [
+    (8, 2, [20, 7, 32], "one Q tile per CTA: key halves"),
+    (8, 2, [70, 33, 100], "two Q tiles per CTA"),
+    (24, 1, [20, 7, 32], "row mode (head group of 24)"),
+])
+def test_prefill_lse_matches_oracle(lk, Hq, Hkv, q_len, path):
+    """The optional log-sum-exp output of the prefill (natural log of the row's softmax
+    denominator over the scaled logits) on each prefill path, against the oracle's."""
+    import torch
+    w = make_custom([200, 37, 1000, 15, 1], [[0, 1, 2], [3, 4, 0], [2]], Hq, Hkv, 128,
+                    PosCfg("rope", 5e5, 128), q_len, 0, seed=61)
+    pb = _batch(w)
+    pb.fill_documents()
+    inp = pb.upload_prefill()
+    lse = torch.full((pb.total_q, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    out = pb.prefill(inp, lse=lse)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    _, meta, _, q_start, doc_blocks = oracle_meta(w)
+    reqs = [0, 1, 2]
+    kc, vc = oracle_caches_for(w, request_instances(w, reqs), prefill=True)
+    ref_o, ref_l = lo.prefill(w.prefill_tokens()[0], w.cu_q, q_start, doc_blocks, meta, kc, vc, w.pos.as_dict(),
+                              requests=reqs)
+    assert_close(out, ref_o, f"prefill output ({path})")
+    err = np.abs(lse.cpu().numpy() - ref_l)
+    assert np.isfinite(err).all(), f"{path}: non-finite log-sum-exp"
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3, f"{path}: lse max-abs {err.max():.3e} mean {err.mean():.3e}"
+
+
 # ------------------------------------------------------------------ poisoned caches
 POISON_CASES = {  # name -> (workload, requests checked, decode steps, steps checked)
     # 32-token queries of a 4-head group: one live Q tile per CTA; 200-token documents end
