@@ -370,10 +370,17 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
                     "avg_launch_us": avg_dec_ms * 1e3}
     else:
         traffic = profiled_traffic("prefill_tc.cu", f"prefill_{name}_{sharing}.md")
-        roofline = {"kernel": "lazy_attn_prefill (tcgen05)", "bound": "tensor", "achieved": pre_tflops,
-                    "peak": bf16_peak, "unit": "TFLOP/s", "frac": pre_tflops / bf16_peak,
-                    "peak_source": f"{peak_kind} bf16_tflops (burst)", "traffic": traffic,
-                    "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_mean * 1e3}
+        roof = prefill_roof(pre_flops, prefill_bytes(w, pb), pre_mean * 1e3, peaks)
+        if roof["bound"] == "tensor":
+            roofline = {"kernel": "lazy_attn_prefill (tcgen05)", "bound": "tensor", "achieved": pre_tflops,
+                        "peak": bf16_peak, "unit": "TFLOP/s", "frac": pre_tflops / bf16_peak,
+                        "peak_source": f"{peak_kind} bf16_tflops (burst)", "traffic": traffic,
+                        "algorithmic_flops_per_launch": pre_flops, "avg_launch_us": pre_mean * 1e3}
+        else:
+            roofline = {"kernel": "lazy_attn_prefill (tcgen05)", "bound": "hbm", "achieved": roof["hbm_gbs"],
+                        "peak": hbm_peak, "unit": "GB/s", "frac": roof["frac_hbm_peak"],
+                        "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                        "algorithmic_bytes_per_launch": prefill_bytes(w, pb), "avg_launch_us": pre_mean * 1e3}
     res = {
         "value": value, "ms_per_step": mean_ms, "tokens_per_step": tokens_per_step,
         "workload": f"{name}: {WORKLOAD_TEXT[name]}" + (f" (first {w.B} requests)" if w.B != make_workload(
@@ -393,7 +400,8 @@ def measure_step(args, dist, lk, name, sharing, steps, warmup, clocks=None, e2e=
             "median_us": pre_med * 1e3 if pre_med else None, "tflops": pre_tflops,
             "frac_bf16_peak": pre_tflops / bf16_peak if pre_tflops else None,
             "hbm_bytes_per_launch": prefill_bytes(w, pb),
-            "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+            "peak_source": f"{peak_kind} bf16_tflops (burst)",
+            **(prefill_roof(pre_flops, prefill_bytes(w, pb), pre_mean * 1e3, peaks) if pre_mean else {})},
         "gpu_launches": launches * steps,
         "wall_s_timed_region": wall,
     }
@@ -423,6 +431,19 @@ def prefill_bytes(w, pb) -> int:
     return keys * w.Hkv * w.D * 2 * 2 + 2 * pb.total_q * w.Hq * w.D * 2
 
 
+def prefill_roof(flops, nbytes, us, peaks):
+    """Which roof bounds a prefill launch: its arithmetic intensity (FLOPs per unique HBM byte)
+    against the ridge of the measured peaks (bf16 FLOP/s over copy bytes/s), and the launch's
+    rate against the HBM roof (for short queries over long contexts the bytes, not the MMAs,
+    set the floor)."""
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    intensity, ridge = flops / nbytes, bf16 * 1e12 / (hbm * 1e9)
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"bound": "tensor" if intensity > ridge else "hbm", "intensity_flop_per_byte": intensity,
+            "ridge_flop_per_byte": ridge, "hbm_gbs": gbs, "frac_hbm_peak": gbs / hbm}
+
+
 def prefill_probe(args, dist, lk, name, sharing):
     """The tensor-core prefill on its own workload (by default the 70B shape, whose prefill is
     a dense contraction): median of eager launches with L2 flushed before each, over the same
@@ -449,6 +470,7 @@ def prefill_probe(args, dist, lk, name, sharing):
             "median_us": ovh["prefill"]["median_us"]["rot"], "tflops": tflops,
             "frac_bf16_peak": tflops / bf16_peak, "peak": bf16_peak,
             "peak_source": f"{peak_kind} bf16_tflops (burst: the kernel is timed on its own)",
+            **prefill_roof(flops, prefill_bytes(w, pb), us, peaks),
             "timing": "eager launches, L2 flushed before each, mean (same runs as rotation_overhead)",
             "traffic": profiled_traffic("prefill_tc.cu", f"prefill_{name}_{sharing}.md"),
             "rotation_overhead": ovh["prefill"] | {"method": ovh["method"],
