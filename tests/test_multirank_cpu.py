@@ -67,3 +67,25 @@ def test_reference_arm_prints_on_rank0_only():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_prefill_roof_by_arithmetic_intensity():
+    """The bench names the roof of a prefill launch by its FLOPs per unique HBM byte against
+    the ridge of the measured peaks: the 70B shape's two 128-row Q tiles per KV head sit above
+    it (tensor-bound), the 32-token RAG and YaRN queries over long contexts below (HBM-bound)."""
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import make_workload
+    peaks = {"bf16_tflops": 1932.3, "hbm_gbs": 6784.5}
+    bounds = {}
+    for name in ("prefill70b", "rag8b", "yarn8b", "mqa_alibi"):
+        w = make_workload(name, sharing="private")
+        q_start = [int(w.inst_len[w.req_inst[w.req_inst_off[b]:w.req_inst_off[b + 1]]].sum()) for b in range(w.B)]
+        pb = types.SimpleNamespace(q_start_h=q_start, total_q=int(w.q_len.sum()))
+        flops, nbytes = bench.prefill_flops(w, pb), bench.prefill_bytes(w, pb)
+        roof = bench.prefill_roof(flops, nbytes, 100.0, peaks)
+        assert abs(roof["ridge_flop_per_byte"] - 1932.3e12 / 6784.5e9) < 1e-9
+        assert abs(roof["hbm_gbs"] - nbytes / 100e-6 / 1e9) < 1e-6 * roof["hbm_gbs"]
+        bounds[name] = roof["bound"]
+    assert bounds == {"prefill70b": "tensor", "rag8b": "hbm", "yarn8b": "hbm", "mqa_alibi": "tensor"}
