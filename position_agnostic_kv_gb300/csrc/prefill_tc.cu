@@ -484,39 +484,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         for (int c = 0; c < NK / 32; ++c)
           tmem_ld32(tS + uint32_t(pg0 * kPage + 32 * c), *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
         tmem_wait_ld();
-        if (POS == kAlibi && fast) {  // bias only: -slope (m - p), p = start + t
+        // ALiBi bias -slope (m - p) for stage row t of a page, p = pstart + t: its per-key part
+        // slope t goes onto the scores in packed pairs, its per-page part slope (pstart - m)
+        // onto the page's maximum and into the page's exponent offset below (one packed FMA per
+        // two scores instead of a multiply-add and an add per score)
+        float bpg[NPG];
+        if constexpr (POS == kAlibi) {
 #pragma unroll
           for (int pp = 0; pp < NPG; ++pp) {
-            const float base = slope * float(pstart[slot * kPagesPerTile + pg0 + pp] - m_row);
+            bpg[pp] = slope * float(pstart[slot * kPagesPerTile + pg0 + pp] - m_row);
 #pragma unroll
-            for (int t = 0; t < kPage; ++t)
-              v[pp * kPage + t] = __float_as_uint(__uint_as_float(v[pp * kPage + t]) + fmaf(slope, float(t), base));
+            for (int t = 0; t < kPage; t += 2) {
+              float2 x = make_float2(__uint_as_float(v[pp * kPage + t]), __uint_as_float(v[pp * kPage + t + 1]));
+              x = __ffma2_rn(make_float2(slope, slope), make_float2(float(t), float(t + 1)), x);
+              v[pp * kPage + t] = __float_as_uint(x.x);
+              v[pp * kPage + t + 1] = __float_as_uint(x.y);
+            }
           }
-        } else if (!fast) {  // stage row t of a page holds key p = pstart + t; visible iff t >= lo, p <= m
+        }
+        if (!fast) {  // stage row t of a page holds key p = pstart + t; visible iff t >= lo, p <= m
 #pragma unroll
           for (int pp = 0; pp < NPG; ++pp) {
             const int st = pstart[slot * kPagesPerTile + pg0 + pp];
             const int lo = pinfo[slot * kPagesPerTile + pg0 + pp].y;
             const int hi = m_row - st + 1;
-            float base = 0.f;
-            if constexpr (POS == kAlibi) base = slope * float(st - m_row);
 #pragma unroll
-            for (int t = 0; t < kPage; ++t) {
-              float x = __uint_as_float(v[pp * kPage + t]);
-              if constexpr (POS == kAlibi) x += fmaf(slope, float(t), base);
-              v[pp * kPage + t] = __float_as_uint((t >= lo && t < hi) ? x : -INFINITY);
-            }
+            for (int t = 0; t < kPage; ++t)
+              if (!(t >= lo && t < hi)) v[pp * kPage + t] = __float_as_uint(-INFINITY);
           }
         }
-        // row max over the scores: independent runs of three-input maxima over 16, then a tree
-        float mq[NK / 16];
+        // row max over the scores: independent runs of three-input maxima over each page's 16,
+        // then a tree
+        float mq[NPG];
 #pragma unroll
-        for (int q = 0; q < NK / 16; ++q) {
+        for (int q = 0; q < NPG; ++q) {
           const float* x = reinterpret_cast<const float*>(v + 16 * q);
           float m = max3f(x[0], x[1], x[2]);
 #pragma unroll
           for (int e = 3; e < 15; e += 2) m = max3f(m, x[e], x[e + 1]);
           mq[q] = fmaxf(m, x[15]);
+          if constexpr (POS == kAlibi) mq[q] += bpg[q];
         }
         float mx;
         if constexpr (KH)
@@ -526,14 +533,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant
         const bool need = mx > m_run + kTau;
         const float m_new = need ? mx : m_run;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // fully masked row: every p is 0
-        const float2 mneg = make_float2(-m_use, -m_use);
+        float2 mneg[NPG];  // exponent offset per page: -m, with ALiBi the page's bias part too
+#pragma unroll
+        for (int pp = 0; pp < NPG; ++pp) {
+          const float o = POS == kAlibi ? bpg[pp] - m_use : -m_use;
+          mneg[pp] = make_float2(o, o);
+        }
         float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};  // four independent partial sums
         // P packed to bf16 pairs in place: pair e (keys 2e, 2e+1) lands in v[e] (already consumed)
 #pragma unroll
         for (int e = 0; e < NK / 2; ++e) {
           float2 x = make_float2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-          x = __fadd2_rn(x, mneg);
+          x = __fadd2_rn(x, mneg[e / (kPage / 2)]);
           const float2 ev = make_float2(ex2(x.x), ex2(x.y));
           sum4[e & 3] = __fadd2_rn(sum4[e & 3], ev);
           v[e] = f2_to_bf2(ev.x, ev.y);
