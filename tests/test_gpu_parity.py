@@ -349,6 +349,39 @@ def test_rope_variants(lk, D, Hq, Hkv, rd, inter, kind, table):
     np.testing.assert_array_equal(_bits(pb.k_cache)[..., rd:], kc[..., rd:])
 
 
+@pytest.mark.parametrize("name,batch", [("rag8b", 2), ("prefill70b", 1)])
+def test_one_key_far_above_the_running_max(lk, name, batch):
+    """The key of each request's first query token replaced by one large component (1024 in
+    the lowest-frequency dimension 63, zeros elsewhere): every query row sees it, and where q's
+    dimension 63 is positive its logit lies up to hundreds of log2 units above the running max
+    taken on the document tiles, so the lazy softmax rescales O and l by a factor that
+    underflows to zero and the row's output becomes that key's value.  A single component
+    keeps the logit's rounding error proportional to the logit (a random key scaled up would
+    carry every component's rounding, scaled, into rows where it only half dominates).  Key
+    halves (rag8b, one Q tile per CTA) and two Q tiles per CTA (prefill70b)."""
+    import torch
+    from position_agnostic_kv_gb300.runner import bits_to_tensor
+    w = make_workload(name, batch=batch)
+    pb = _batch(w)
+    pb.fill_documents()
+    q, k, v, slot, lp = w.prefill_tokens()
+    k64 = k.copy()
+    first = w.cu_q[:-1][w.q_len > 0]
+    k64[first] = 0
+    k64[first, :, 63] = f32_to_bf16_bits(np.full((len(first), w.Hkv), 1024.0, np.float32))
+    inp = pb.upload_prefill()
+    inp["k"] = bits_to_tensor(k64, inp["k"].device)
+    out = pb.prefill(inp)
+    torch.cuda.synchronize()
+    _status_clean(lk)
+    _, meta, _, qs, db = oracle_meta(w)
+    pos = w.pos.as_dict()
+    kc, vc = oracle_caches_for(w, prefill=False)
+    oracle.kv_write(k64, v, slot, lp, pos, kc, vc)
+    ref, _ = lo.prefill(q, w.cu_q, qs, db, meta, kc, vc, pos)
+    assert_close(out, ref, f"{name} prefill, one key far above the running max")
+
+
 def test_sharpened_queries_separate_negative_controls(lk):
     """With queries x4 the softmax is sharp: the GPU output must match the oracle, while the
     oracle run with wrong offsets (Delta = 0 everywhere, Delta + 1, the naive double rotation
