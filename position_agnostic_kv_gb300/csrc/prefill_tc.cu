@@ -45,7 +45,9 @@
 // GQA: a tile's rows are (token, head) pairs of the KV head's query-head group, token-major.
 // Decode mode serves wide head groups (MQA): the G heads of one new token fill the rows, the
 // key range is split over several CTAs and their partials are merged by log-sum-exp.
-// With ALiBi the tiles are visited newest first (the running max is fixed by the first tile).
+// With ALiBi the tiles are visited newest first (the running max is fixed by the first tile),
+// and the bias -slope (m - p) is split into slope t per key row t of a page (a packed FMA on
+// the scores) and slope (pstart - m) per page (on the page's max and its exponent offset).
 // Every wait is bounded (mbarrier polls against %globaltimer; an abort flag ends all roles).
 // Warp 15 has no role, nor has warp 14 outside SPLIT_V (or warps 4-7 of a CTA with one live
 // Q tile outside KH).
